@@ -1,0 +1,28 @@
+"""GB300-native fused LM-head GRPO / GSPO loss.
+
+The compute lives in ``libgrpohead.so`` (hand-written sm_103a CUDA: tcgen05
+tensor-core tiles fed by TMA, online fp32 log-sum-exp over the vocabulary,
+GRPO/GSPO epilogues).  This package is a thin ctypes binding with the same
+entry-point names as the C ABI in ``include/grpo_head.h``:
+
+    grpo_head_forward, gspo_segment_loss, grpo_head_backward, grpo_group_advantage
+
+The binding is imported lazily so that ``import gspo_logprob_gb300`` works on a
+machine without the built library; the first call then fails loudly if the
+library is missing.
+"""
+__all__ = ["grpo_head_forward", "gspo_segment_loss", "grpo_head_backward", "grpo_group_advantage",
+           "build", "ops"]
+
+
+def build(verbose: bool = False) -> str:
+    from .build import build as _build
+    return _build(verbose=verbose)
+
+
+def __getattr__(name):
+    if name in ("grpo_head_forward", "gspo_segment_loss", "grpo_head_backward", "grpo_group_advantage", "ops"):
+        import importlib
+        ops = importlib.import_module(".ops", __name__)
+        return ops if name == "ops" else getattr(ops, name)
+    raise AttributeError(name)

@@ -1,0 +1,457 @@
+// C ABI of the fused LM-head GRPO / GSPO loss: argument validation, workspace
+// layout, launch sequencing and the optional per-kernel event instrumentation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "grpo_head.h"
+#include "internal.h"
+
+namespace gh {
+
+static thread_local std::string g_last_error;
+
+static gh_status fail(gh_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+static gh_status fail(gh_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+static gh_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- device facts
+static std::mutex g_mu;
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+static bool device_is_sm103() {
+  static int cache[64] = {0};  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev < 0 || dev >= 64) return false;
+  if (cache[dev] == 0) {
+    int ma = 0, mi = 0;
+    cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev);
+    cache[dev] = (ma == 10 && mi == 3) ? 1 : 2;
+  }
+  return cache[dev] == 1;
+}
+
+uint64_t timeout_ns() {
+  static uint64_t t = 0;
+  if (t == 0) {
+    const char* e = getenv("GH_TIMEOUT_NS");
+    unsigned long long v = e ? strtoull(e, nullptr, 10) : 0ull;
+    t = v > 0 ? v : 2000000000ull;  // 2 s
+  }
+  return t;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                    uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- instrumentation
+struct Prof {
+  bool on = false;
+  int64_t launches_total = 0;
+  struct Rec {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  size_t pool_next = 0;
+  int64_t count[GH_NUM_KERNEL_KINDS] = {0};
+  double ms[GH_NUM_KERNEL_KINDS] = {0};
+};
+static Prof g_prof;
+
+static cudaEvent_t pool_event() {
+  if (g_prof.pool_next < g_prof.pool.size()) return g_prof.pool[g_prof.pool_next++];
+  cudaEvent_t e;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  g_prof.pool.push_back(e);
+  g_prof.pool_next = g_prof.pool.size();
+  return e;
+}
+
+template <class F>
+static cudaError_t run(int kind, cudaStream_t st, F&& f) {
+  ++g_prof.launches_total;
+  if (!g_prof.on) return f();
+  cudaEvent_t a = pool_event(), b = pool_event();
+  if (a) cudaEventRecord(a, st);
+  cudaError_t e = f();
+  if (b) cudaEventRecord(b, st);
+  if (a && b) g_prof.recs.push_back({kind, a, b});
+  return e;
+}
+
+static void prof_collect() {
+  for (auto& r : g_prof.recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      g_prof.count[r.kind] += 1;
+      g_prof.ms[r.kind] += ms;
+    }
+  }
+  g_prof.recs.clear();
+  g_prof.pool_next = 0;
+}
+
+// ---------------------------------------------------------------- validation helpers
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static gh_status check_head(const gh_head* h) {
+  if (!h) return fail(GH_ERR_INVALID_ARG, "head is NULL");
+  if (h->N < 0 || h->N > (int64_t(1) << 30)) return fail(GH_ERR_INVALID_ARG, "N=%lld out of range", (long long)h->N);
+  if (h->D < 1 || h->D > (int64_t(1) << 20)) return fail(GH_ERR_INVALID_ARG, "D=%lld out of range", (long long)h->D);
+  if (h->V < 1 || h->V > (int64_t(1) << 28)) return fail(GH_ERR_INVALID_ARG, "V=%lld out of range", (long long)h->V);
+  if (h->dtype != GH_BF16 && h->dtype != GH_FP32) return fail(GH_ERR_INVALID_ARG, "dtype=%d unknown", h->dtype);
+  if (h->row_tile != 0 && h->row_tile != 64 && h->row_tile != 128 && h->row_tile != 256)
+    return fail(GH_ERR_INVALID_ARG, "row_tile=%d (expected 0, 64, 128 or 256)", h->row_tile);
+  if (!h->W) return fail(GH_ERR_INVALID_ARG, "W is NULL");
+  if (h->N > 0 && (!h->H || !h->targets || !h->mask)) return fail(GH_ERR_INVALID_ARG, "H/targets/mask is NULL");
+  if (h->dtype == GH_BF16) {
+    if (h->D % 8 != 0) return fail(GH_ERR_INVALID_ARG, "bf16 needs D %% 8 == 0 (D=%lld)", (long long)h->D);
+    if (!aligned16(h->W) || (h->N > 0 && !aligned16(h->H)))
+      return fail(GH_ERR_INVALID_ARG, "bf16 H and W must be 16-byte aligned");
+  } else {
+    if (!aligned16(h->W) || (h->N > 0 && !aligned16(h->H)))
+      return fail(GH_ERR_INVALID_ARG, "fp32 H and W must be 16-byte aligned");
+  }
+  return GH_OK;
+}
+
+static int64_t num_splits(int64_t V) { return ceil_div(ceil_div(V, VTILE), TILES_PER_SPLIT); }
+
+struct FwdWs {
+  float* part_m;
+  float* part_s;
+  float* zy;
+  size_t bytes;
+};
+static FwdWs fwd_layout(const gh_head* h, void* base) {
+  const int64_t S = num_splits(h->V), N = h->N;
+  const size_t a = align_up(static_cast<size_t>(S * N) * 4, 256);
+  const size_t z = align_up(static_cast<size_t>(N) * 4, 256);
+  char* b = static_cast<char*>(base);
+  FwdWs w;
+  w.part_m = reinterpret_cast<float*>(b);
+  w.part_s = reinterpret_cast<float*>(b + a);
+  w.zy = reinterpret_cast<float*>(b + 2 * a);
+  w.bytes = 2 * a + z;
+  return w;
+}
+
+struct BwdWs {
+  void* G;
+  float* acc32;
+  int64_t vb;     // block width (columns)
+  int64_t nblk;   // blocks
+  size_t bytes;
+};
+static BwdWs bwd_layout(const gh_head* h, void* base) {
+  const int64_t Vp = ceil_div(h->V, VTILE) * VTILE;
+  BwdWs w;
+  w.vb = Vp < BWD_BLOCK_COLS ? Vp : BWD_BLOCK_COLS;
+  w.nblk = ceil_div(Vp, w.vb);
+  const size_t elt = h->dtype == GH_BF16 ? 2 : 4;
+  const size_t g = align_up(static_cast<size_t>(h->N) * w.vb * elt, 256);
+  const size_t acc = (h->dtype == GH_BF16 && w.nblk > 1) ? align_up(static_cast<size_t>(h->N) * h->D * 4, 256) : 0;
+  char* b = static_cast<char*>(base);
+  w.G = b;
+  w.acc32 = acc ? reinterpret_cast<float*>(b + g) : nullptr;
+  w.bytes = g + acc;
+  return w;
+}
+
+}  // namespace gh
+
+using namespace gh;
+
+extern "C" {
+
+int32_t gh_abi_version(void) { return 100; }
+
+const char* gh_status_string(gh_status s) {
+  switch (s) {
+    case GH_OK: return "GH_OK";
+    case GH_ERR_INVALID_ARG: return "GH_ERR_INVALID_ARG";
+    case GH_ERR_UNSUPPORTED: return "GH_ERR_UNSUPPORTED";
+    case GH_ERR_WORKSPACE: return "GH_ERR_WORKSPACE";
+    case GH_ERR_CUDA: return "GH_ERR_CUDA";
+  }
+  return "GH_ERR_UNKNOWN";
+}
+
+const char* gh_last_error(void) { return g_last_error.c_str(); }
+
+size_t grpo_head_forward_workspace_size(const gh_head* head) {
+  if (check_head(head) != GH_OK) return 0;
+  return fwd_layout(head, nullptr).bytes;
+}
+
+size_t grpo_head_backward_workspace_size(const gh_head* head) {
+  if (check_head(head) != GH_OK) return 0;
+  return bwd_layout(head, nullptr).bytes;
+}
+
+gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* logp, float* lse, float* coef,
+                            float* loss3, int32_t* status, void* ws, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  gh_status s = check_head(head);
+  if (s != GH_OK) return s;
+  if (!status) return fail(GH_ERR_INVALID_ARG, "status is NULL");
+  if (head->N > 0 && (!logp || !lse)) return fail(GH_ERR_INVALID_ARG, "logp/lse is NULL");
+  if ((coef || loss3) && !grpo) return fail(GH_ERR_INVALID_ARG, "coef/loss3 requested without GRPO parameters");
+  if (grpo) {
+    if (head->N > 0 && (!grpo->old_logp || !grpo->adv || !grpo->seq_id))
+      return fail(GH_ERR_INVALID_ARG, "old_logp/adv/seq_id is NULL");
+    if (!grpo->ref_logp && grpo->beta != 0.f) return fail(GH_ERR_INVALID_ARG, "ref_logp is NULL with beta != 0");
+    if (grpo->num_seqs < 1 || grpo->num_seqs > MAX_SEQS)
+      return fail(GH_ERR_INVALID_ARG, "num_seqs=%d out of [1, %d]", grpo->num_seqs, MAX_SEQS);
+    if (grpo->reduction < GH_TOKEN_MEAN || grpo->reduction > GH_FIXED)
+      return fail(GH_ERR_INVALID_ARG, "reduction=%d unknown", grpo->reduction);
+    if (grpo->reduction == GH_FIXED && !(grpo->norm > 0.0))
+      return fail(GH_ERR_INVALID_ARG, "fixed reduction needs norm > 0");
+    if (!(grpo->eps_low >= 0.f) || !(grpo->eps_high >= 0.f) || !std::isfinite(grpo->beta) || grpo->norm < 0.0)
+      return fail(GH_ERR_INVALID_ARG, "eps_low/eps_high/beta/norm invalid");
+  }
+  const size_t need = fwd_layout(head, nullptr).bytes;
+  if (need > 0 && (!ws || ws_bytes < need))
+    return fail(GH_ERR_WORKSPACE, "forward workspace needs %zu bytes, got %zu", need, ws ? ws_bytes : size_t(0));
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int N = static_cast<int>(head->N), D = static_cast<int>(head->D), V = static_cast<int>(head->V);
+  if (N > 0) {
+    FwdWs w = fwd_layout(head, ws);
+    cudaError_t e;
+    if (head->dtype == GH_BF16) {
+      TcFwdArgs a{N, D, V, head->row_tile, head->H, head->W, head->targets, w.part_m, w.part_s, w.zy, status};
+      e = run(K_FWD_TC, st, [&] { return launch_fwd_tc(a, st); });
+    } else {
+      F32FwdArgs a{N, D, V, head->row_tile, static_cast<const float*>(head->H), static_cast<const float*>(head->W),
+                   head->targets, w.part_m, w.part_s, w.zy};
+      e = run(K_FWD_F32, st, [&] { return launch_fwd_f32(a, st); });
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "forward logits/LSE launch");
+    e = run(K_MERGE, st, [&] {
+      return launch_merge(N, V, static_cast<int>(num_splits(V)), w.part_m, w.part_s, w.zy, head->targets, head->mask,
+                          logp, lse, status, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
+  if (grpo) {
+    cudaError_t e = run(K_GRPO, st, [&] { return launch_grpo(N, logp, head->mask, grpo, coef, loss3, status, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "GRPO loss launch");
+  }
+  return GH_OK;
+}
+
+gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp, const uint8_t* mask,
+                            const int32_t* seg_id, int32_t num_segments, const float* seg_adv, float eps_low,
+                            float eps_high, double divisor, int32_t token_weighted, float* loss, float* seg_ratio,
+                            float* coef, float* mean_logp, int32_t* status, void* stream) {
+  g_last_error.clear();
+  if (N < 0 || N > (int64_t(1) << 30)) return fail(GH_ERR_INVALID_ARG, "N out of range");
+  if (!status || !loss || !seg_adv) return fail(GH_ERR_INVALID_ARG, "status/loss/seg_adv is NULL");
+  if (N > 0 && (!logp || !old_logp || !mask || !seg_id || !coef))
+    return fail(GH_ERR_INVALID_ARG, "logp/old_logp/mask/seg_id/coef is NULL");
+  if (num_segments < 1 || num_segments > MAX_SEQS)
+    return fail(GH_ERR_INVALID_ARG, "num_segments=%d out of [1, %d]", num_segments, MAX_SEQS);
+  if (!(divisor > 0.0) || !std::isfinite(divisor)) return fail(GH_ERR_INVALID_ARG, "divisor must be > 0");
+  if (!(eps_low >= 0.f) || !(eps_high >= 0.f)) return fail(GH_ERR_INVALID_ARG, "eps must be >= 0");
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = run(K_GSPO, st, [&] {
+    return launch_gspo(static_cast<int>(N), logp, old_logp, mask, seg_id, num_segments, seg_adv, eps_low, eps_high,
+                       divisor, token_weighted, loss, seg_ratio, coef, mean_logp, status, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "GSPO launch");
+  return GH_OK;
+}
+
+gh_status grpo_head_backward(const gh_head* head, const float* lse, const float* coef, const float* grad_out,
+                             void* dH, float* dW, int32_t accumulate_dW, int32_t* status, void* ws, size_t ws_bytes,
+                             void* stream) {
+  g_last_error.clear();
+  gh_status s = check_head(head);
+  if (s != GH_OK) return s;
+  if (!status || !dW) return fail(GH_ERR_INVALID_ARG, "status/dW is NULL");
+  if (head->N > 0 && (!lse || !coef || !dH)) return fail(GH_ERR_INVALID_ARG, "lse/coef/dH is NULL");
+  if (!aligned16(dW) || (head->N > 0 && !aligned16(dH))) return fail(GH_ERR_INVALID_ARG, "dH/dW must be 16-byte aligned");
+  const size_t need = bwd_layout(head, nullptr).bytes;
+  if (need > 0 && (!ws || ws_bytes < need))
+    return fail(GH_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", need, ws ? ws_bytes : size_t(0));
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int N = static_cast<int>(head->N), D = static_cast<int>(head->D), V = static_cast<int>(head->V);
+  if (N == 0) {
+    if (!accumulate_dW) {
+      cudaError_t e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * D * sizeof(float), st);
+      if (e != cudaSuccess) return cuda_fail(e, "dW clear");
+    }
+    return GH_OK;
+  }
+  BwdWs w = bwd_layout(head, ws);
+  const int64_t Vp = ceil_div(V, VTILE) * VTILE;
+  for (int64_t b = 0; b < w.nblk; ++b) {
+    const int vb0 = static_cast<int>(b * w.vb);
+    const int width = static_cast<int>((Vp - vb0) < w.vb ? (Vp - vb0) : w.vb);
+    const int ldg = static_cast<int>(w.vb);
+    cudaError_t e;
+    if (head->dtype == GH_BF16) {
+      TcDlogitsArgs da{N, D, V, vb0, width, ldg, head->H, head->W, head->targets, lse, coef, grad_out, w.G, status};
+      e = run(K_DLOGITS_TC, st, [&] { return launch_dlogits_tc(da, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
+      int mode;
+      if (w.nblk == 1)
+        mode = 3;
+      else if (b == 0)
+        mode = 0;
+      else if (b == w.nblk - 1)
+        mode = 2;
+      else
+        mode = 1;
+      TcDhArgs ha{N, D, V, vb0, width, ldg, w.G, head->W, mode, w.acc32, dH, status};
+      e = run(K_DH_TC, st, [&] { return launch_dh_tc(ha, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "dH launch");
+      TcDwArgs wa{N, D, V, vb0, width, ldg, w.G, head->H, accumulate_dW, dW, status};
+      e = run(K_DW_TC, st, [&] { return launch_dw_tc(wa, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "dW launch");
+    } else {
+      const float* H = static_cast<const float*>(head->H);
+      const float* W = static_cast<const float*>(head->W);
+      float* G = static_cast<float*>(w.G);
+      F32DlogitsArgs da{N, D, V, vb0, width, ldg, H, W, head->targets, lse, coef, grad_out, G};
+      e = run(K_DLOGITS_F32, st, [&] { return launch_dlogits_f32(da, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
+      const int real = static_cast<int>((V - vb0) < width ? (V - vb0) : width);
+      // dH[N, D] (+)= G[:, :real] W[vb0:vb0+real, :]
+      F32GemmArgs ha{N, D, real, G, ldg, 1, W + static_cast<size_t>(vb0) * D, D, 1, static_cast<float*>(dH), D, 0,
+                     b > 0 ? 1 : 0};
+      e = run(K_GEMM_F32, st, [&] { return launch_gemm_f32(ha, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "dH launch");
+      // dW[vb0 + v, :] (+)= sum_i G[i, v] H[i, :]
+      F32GemmArgs wa{real, D, N, G, 1, ldg, H, D, 1, dW, D, vb0, accumulate_dW ? 1 : 0};
+      e = run(K_GEMM_F32, st, [&] { return launch_gemm_f32(wa, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "dW launch");
+    }
+  }
+  return GH_OK;
+}
+
+gh_status grpo_group_advantage(const float* rewards, int32_t num_seqs, int32_t group_size, float eps, float* adv,
+                               int32_t* status, void* stream) {
+  g_last_error.clear();
+  if (!rewards || !adv || !status) return fail(GH_ERR_INVALID_ARG, "rewards/adv/status is NULL");
+  if (group_size < 1 || num_seqs < 1 || num_seqs % group_size != 0)
+    return fail(GH_ERR_INVALID_ARG, "num_seqs=%d must be a positive multiple of group_size=%d", num_seqs, group_size);
+  if (!(eps >= 0.f)) return fail(GH_ERR_INVALID_ARG, "eps must be >= 0");
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      run(K_ADV, st, [&] { return launch_advantage(rewards, num_seqs, group_size, eps, adv, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "advantage launch");
+  return GH_OK;
+}
+
+void gh_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof.on = on != 0;
+}
+
+void gh_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  prof_collect();
+  for (int k = 0; k < GH_NUM_KERNEL_KINDS; ++k) {
+    g_prof.count[k] = 0;
+    g_prof.ms[k] = 0.0;
+  }
+}
+
+gh_status gh_profile_read(int32_t kind, int64_t* launches, double* total_ms) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (kind < 0 || kind >= GH_NUM_KERNEL_KINDS || !launches || !total_ms)
+    return fail(GH_ERR_INVALID_ARG, "bad profile query");
+  prof_collect();
+  *launches = g_prof.count[kind];
+  *total_ms = g_prof.ms[kind];
+  return GH_OK;
+}
+
+int64_t gh_launch_count(void) { return g_prof.launches_total; }
+
+const char* gh_kernel_kind_name(int32_t kind) {
+  static const char* names[GH_NUM_KERNEL_KINDS] = {
+      "fwd_logits_lse_tc", "merge_lse", "grpo_loss", "gspo_segment", "dlogits_tc", "dh_gemm_tc",
+      "dw_gemm_tc", "group_advantage", "fwd_logits_lse_f32", "dlogits_f32", "gemm_f32", "timeout_probe"};
+  if (kind < 0 || kind >= GH_NUM_KERNEL_KINDS) return "";
+  return names[kind];
+}
+
+gh_status gh_timeout_probe(int32_t* status, uint64_t timeout_ns_, void* stream) {
+  g_last_error.clear();
+  if (!status) return fail(GH_ERR_INVALID_ARG, "status is NULL");
+  if (timeout_ns_ == 0 || timeout_ns_ > 10000000000ull) return fail(GH_ERR_INVALID_ARG, "timeout out of (0, 10 s]");
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = run(K_PROBE, st, [&] { return launch_timeout_probe(status, timeout_ns_, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "probe launch");
+  return GH_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,152 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "grpo_head.h"
+
+namespace gh {
+
+// Column tiling of the vocabulary: 256-column tiles, TILES_PER_SPLIT tiles per
+// split.  The split count depends on V only, which keeps logp/LSE bitwise
+// independent of N, the row tile and the GPU's SM count.
+constexpr int VTILE = 256;
+constexpr int TILES_PER_SPLIT = 4;
+constexpr int SPLIT_COLS = VTILE * TILES_PER_SPLIT;
+// Backward vocabulary block (columns of dlogits held in the workspace at once).
+constexpr int BWD_BLOCK_COLS = 4096;
+// Maximum sequences / segments handled by the single-CTA loss kernels.
+constexpr int MAX_SEQS = 16384;
+
+enum KernelKind {
+  K_FWD_TC = 0,
+  K_MERGE = 1,
+  K_GRPO = 2,
+  K_GSPO = 3,
+  K_DLOGITS_TC = 4,
+  K_DH_TC = 5,
+  K_DW_TC = 6,
+  K_ADV = 7,
+  K_FWD_F32 = 8,
+  K_DLOGITS_F32 = 9,
+  K_GEMM_F32 = 10,
+  K_PROBE = 11,
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct TmapPair {
+  CUtensorMap a, b;
+};
+
+// bf16 2-D tensor map (row-major [outer, inner], row stride in bytes), 128-byte
+// swizzle, zero fill out of bounds.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+int num_sms();
+uint64_t timeout_ns();
+
+// --- tcgen05 launchers (tc_kernels.cu) ---------------------------------------
+struct TcFwdArgs {
+  int N, D, V, row_tile;
+  const void* H;
+  const void* W;
+  const int32_t* targets;
+  float* part_m;
+  float* part_s;
+  float* zy;
+  int* status;
+};
+cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st);
+
+struct TcDlogitsArgs {
+  int N, D, V, vb0, width, ldg;
+  const void* H;
+  const void* W;
+  const int32_t* targets;
+  const float* lse;
+  const float* coef;
+  const float* grad_out;
+  void* G;
+  int* status;
+};
+cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st);
+
+struct TcDhArgs {  // dH (+)= G[:, :width] W[vb0:vb0+width, :]
+  int N, D, V, vb0, width, ldg;
+  const void* G;
+  const void* W;
+  int mode;  // EpiStore mode
+  float* acc32;
+  void* out16;
+  int* status;
+};
+cudaError_t launch_dh_tc(const TcDhArgs& a, cudaStream_t st);
+
+struct TcDwArgs {  // dW[vb0:vb0+width] (+)= G[:, :width]^T H
+  int N, D, V, vb0, width, ldg;
+  const void* G;
+  const void* H;
+  int accumulate;
+  float* dW;
+  int* status;
+};
+cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st);
+
+// --- fp32 SIMT launchers (simt_kernels.cu) ----------------------------------
+struct F32FwdArgs {
+  int N, D, V, row_tile;
+  const float* H;
+  const float* W;
+  const int32_t* targets;
+  float* part_m;
+  float* part_s;
+  float* zy;
+};
+cudaError_t launch_fwd_f32(const F32FwdArgs& a, cudaStream_t st);
+
+struct F32DlogitsArgs {
+  int N, D, V, vb0, width, ldg;
+  const float* H;
+  const float* W;
+  const int32_t* targets;
+  const float* lse;
+  const float* coef;
+  const float* grad_out;
+  float* G;
+};
+cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st);
+
+// C[row_off + m, n] (+)= sum_k A(m,k) B(k,n),  A(m,k) = A[m*sam + k*sak], B(k,n) = B[k*sbk + n*sbn]
+struct F32GemmArgs {
+  int M, Nn, K;
+  const float* A;
+  long long sam, sak;
+  const float* B;
+  long long sbk, sbn;
+  float* C;
+  long long ldc;
+  int row_off;
+  int accumulate;
+};
+cudaError_t launch_gemm_f32(const F32GemmArgs& a, cudaStream_t st);
+
+// --- loss kernels (loss_kernels.cu) -----------------------------------------
+cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const float* part_s, const float* zy,
+                         const int32_t* targets, const uint8_t* mask, float* logp, float* lse, int* status,
+                         cudaStream_t st);
+cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_grpo* g, float* coef,
+                        float* loss3, int* status, cudaStream_t st);
+cudaError_t launch_gspo(int N, const float* logp, const float* old_logp, const uint8_t* mask,
+                        const int32_t* seg_id, int num_segments, const float* seg_adv, float eps_low,
+                        float eps_high, double divisor, int token_weighted, float* loss, float* seg_ratio,
+                        float* coef, float* mean_logp, int* status, cudaStream_t st);
+cudaError_t launch_advantage(const float* rewards, int num_seqs, int group_size, float eps, float* adv,
+                             cudaStream_t st);
+cudaError_t launch_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace gh

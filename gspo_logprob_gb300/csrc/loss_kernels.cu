@@ -1,0 +1,491 @@
+// O(N) kernels: split merge -> LSE / logp, the GRPO token objective and its
+// reductions, the GSPO segment seam, group-normalised advantages, and the
+// bounded-wait self-test.  All sums run in a fixed order (lane-strided partial
+// sums in token order, then a xor butterfly or a fixed shared-memory tree), so
+// results are deterministic without floating-point atomics.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gh {
+
+namespace {
+
+__device__ __forceinline__ float wsum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int wsum_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// first index in [lo, hi) with key[idx] >= v (key nondecreasing on [lo, hi))
+__device__ __forceinline__ int lower_bound_i(const int* key, int lo, int hi, int v) {
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (key[mid] < v)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------- merge
+// LSE_i = M + log(sum_k s_k e^{m_k - M}) over splits k in increasing order.
+__global__ void merge_kernel(int N, int V, int splits, const float* __restrict__ part_m,
+                             const float* __restrict__ part_s, const float* __restrict__ zy,
+                             const int* __restrict__ targets, const uint8_t* __restrict__ mask, float* logp,
+                             float* lse, int* status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  float M = -INFINITY;
+  for (int k = 0; k < splits; ++k) M = fmaxf(M, part_m[static_cast<size_t>(k) * N + i]);
+  float S = 0.f;
+  if (M != -INFINITY) {
+    for (int k = 0; k < splits; ++k) {
+      const float mk = part_m[static_cast<size_t>(k) * N + i];
+      if (mk != -INFINITY) S += part_s[static_cast<size_t>(k) * N + i] * expf(mk - M);
+    }
+  }
+  const float L = M + logf(S);
+  lse[i] = L;
+  const int y = targets[i];
+  const bool act = mask[i] != 0;
+  float lp;
+  if (y >= 0 && y < V) {
+    lp = zy[i] - L;
+  } else if (act) {
+    lp = __int_as_float(0x7fc00000);
+    atomicOr(status, GH_DEV_TARGET_OOR);
+  } else {
+    lp = 0.f;
+  }
+  logp[i] = lp;
+  if (!isfinite(L) || (act && y >= 0 && y < V && !isfinite(lp))) atomicOr(status, GH_DEV_NONFINITE);
+}
+
+// ---------------------------------------------------------------- GRPO
+struct GrpoP {
+  int N;
+  const float* logp;
+  const float* old_logp;
+  const float* ref_logp;
+  const float* adv;
+  const int* seq_id;
+  const uint8_t* mask;
+  int num_seqs;
+  int reduction;
+  float eps_low, eps_high, beta;
+  double norm;
+  float* coef;
+  float* loss3;
+  int* status;
+};
+
+struct TokTerms {
+  float r, pg, kl, d;
+  bool act;
+};
+
+__device__ __forceinline__ TokTerms grpo_terms(float lp, float od, float rf, float A, float lo, float hi) {
+  TokTerms t;
+  t.r = expf(lp - od);
+  const float c = fminf(fmaxf(t.r, lo), hi);
+  t.pg = -fminf(t.r * A, c * A);
+  t.d = rf - lp;
+  t.kl = expm1f(t.d) - t.d;  // exp(d) - d - 1
+  t.act = A >= 0.f ? (t.r <= hi) : (t.r >= lo);
+  return t;
+}
+
+// one CTA of 1024 threads; dynamic shared memory: 3 * num_seqs words
+__global__ void __launch_bounds__(1024) grpo_kernel(GrpoP p) {
+  extern __shared__ float sh[];
+  float* sP = sh;
+  float* sK = sh + p.num_seqs;
+  int* sN = reinterpret_cast<int*>(sh + 2 * p.num_seqs);
+  __shared__ float s_scale_tok;  // token_mean / fixed scale, or 1/L for seq_mean
+  __shared__ int s_flag;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nw = blockDim.x >> 5;
+  const float lo = 1.f - p.eps_low, hi = 1.f + p.eps_high;
+
+  // phase 0: layout check -- ids in range and nondecreasing
+  bool bad = false;
+  for (int i = t; i < p.N; i += blockDim.x) {
+    const int s = p.seq_id[i];
+    if (s < 0 || s >= p.num_seqs) bad = true;
+    if (i > 0 && p.seq_id[i - 1] > s) bad = true;
+  }
+  if (__syncthreads_or(bad)) {
+    if (t == 0) {
+      atomicOr(p.status, GH_DEV_BAD_SEQ);
+      if (p.loss3) p.loss3[0] = p.loss3[1] = p.loss3[2] = __int_as_float(0x7fc00000);
+    }
+    if (p.coef)
+      for (int i = t; i < p.N; i += blockDim.x) p.coef[i] = 0.f;
+    return;
+  }
+
+  // phase 1: per-sequence totals of m*pg, m*kl and active counts (warp per sequence)
+  bool nonfinite = false;
+  for (int s = warp; s < p.num_seqs; s += nw) {
+    const int b = lower_bound_i(p.seq_id, 0, p.N, s);
+    const int e = lower_bound_i(p.seq_id, b, p.N, s + 1);
+    const float A = p.adv[s];
+    float ap = 0.f, ak = 0.f;
+    int an = 0;
+    for (int i = b + lane; i < e; i += 32) {
+      if (!p.mask[i]) continue;
+      const float lp = p.logp[i];
+      const TokTerms tt = grpo_terms(lp, p.old_logp[i], p.ref_logp ? p.ref_logp[i] : lp, A, lo, hi);
+      ap += tt.pg;
+      ak += tt.kl;
+      an += 1;
+      if (!isfinite(tt.pg) || !isfinite(tt.kl)) nonfinite = true;
+    }
+    ap = wsum(ap);
+    ak = wsum(ak);
+    an = wsum_i(an);
+    if (lane == 0) {
+      sP[s] = ap;
+      sK[s] = ak;
+      sN[s] = an;
+    }
+  }
+  if (nonfinite) atomicOr(p.status, GH_DEV_NONFINITE);
+  __syncthreads();
+
+  // phase 2 (warp 0): normaliser, then policy/kl = sum_s total_s * scale_s in sequence order
+  if (warp == 0) {
+    long long tot = 0;
+    int live = 0;
+    for (int s = lane; s < p.num_seqs; s += 32) {
+      tot += sN[s];
+      live += sN[s] > 0 ? 1 : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      live += __shfl_xor_sync(0xffffffffu, live, o);
+    }
+    float scale = 0.f;
+    int flag = 0;
+    if (p.reduction == GH_TOKEN_MEAN) {
+      const double den = p.norm > 0.0 ? p.norm : static_cast<double>(tot);
+      if (den > 0.0)
+        scale = static_cast<float>(1.0 / den);
+      else
+        flag = 1;
+    } else if (p.reduction == GH_SEQ_MEAN) {
+      const double den = p.norm > 0.0 ? p.norm : static_cast<double>(live);
+      if (den > 0.0)
+        scale = static_cast<float>(1.0 / den);
+      else
+        flag = 1;
+    } else {
+      scale = static_cast<float>(1.0 / p.norm);
+    }
+    float pol = 0.f, kl = 0.f;
+    if (!flag) {
+      for (int s = lane; s < p.num_seqs; s += 32) {
+        float w = scale;
+        if (p.reduction == GH_SEQ_MEAN) w = sN[s] > 0 ? scale / static_cast<float>(sN[s]) : 0.f;
+        pol += sP[s] * w;
+        kl += sK[s] * w;
+      }
+      pol = wsum(pol);
+      kl = wsum(kl);
+    }
+    if (lane == 0) {
+      s_scale_tok = scale;
+      s_flag = flag;
+      if (flag) atomicOr(p.status, GH_DEV_NO_ACTIVE);
+      if (p.loss3) {
+        p.loss3[0] = pol + p.beta * kl;
+        p.loss3[1] = pol;
+        p.loss3[2] = kl;
+      }
+    }
+  }
+  __syncthreads();
+
+  // phase 3: coef_i = w_i (-A r act + beta (1 - exp(d)))
+  if (p.coef) {
+    const float scale = s_scale_tok;
+    const int flag = s_flag;
+    for (int i = t; i < p.N; i += blockDim.x) {
+      float c = 0.f;
+      if (p.mask[i] && !flag) {
+        const int s = p.seq_id[i];
+        const float A = p.adv[s];
+        const float lp = p.logp[i];
+        const TokTerms tt = grpo_terms(lp, p.old_logp[i], p.ref_logp ? p.ref_logp[i] : lp, A, lo, hi);
+        const float w = p.reduction == GH_SEQ_MEAN ? scale / static_cast<float>(sN[s]) : scale;
+        c = w * (-A * tt.r * (tt.act ? 1.f : 0.f) - p.beta * expm1f(tt.d));
+      }
+      p.coef[i] = c;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- GSPO
+struct GspoP {
+  int N;
+  const float* logp;
+  const float* old_logp;
+  const uint8_t* mask;
+  const int* seg_id;
+  int num_segments;
+  const float* seg_adv;
+  float eps_low, eps_high;
+  double divisor;
+  int token_weighted;
+  float* loss;
+  float* seg_ratio;
+  float* coef;
+  float* mean_logp;
+  int* status;
+};
+
+// one CTA of 1024 threads; dynamic shared memory: 2 * num_segments floats
+__global__ void __launch_bounds__(1024) gspo_kernel(GspoP p) {
+  extern __shared__ float sh[];
+  float* sL = sh;                     // omega_s l_s / divisor
+  float* sG = sh + p.num_segments;    // d loss / d logp for an active token of s
+  __shared__ float red_a[32], red_b[32];
+  __shared__ int s_nvalid;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nw = blockDim.x >> 5;
+  const float lo = 1.f - p.eps_low, hi = 1.f + p.eps_high;
+  const float inv_div = static_cast<float>(1.0 / p.divisor);
+
+  // phase 0: layout -- ids in [-1, S); ids >= 0 nondecreasing; -1 only as a tail, with mask 0
+  bool bad = false;
+  for (int i = t; i < p.N; i += blockDim.x) {
+    const int s = p.seg_id[i];
+    if (s < -1 || s >= p.num_segments) bad = true;
+    if (s < 0 && p.mask[i]) bad = true;
+    if (i > 0) {
+      const int q = p.seg_id[i - 1];
+      if (q < 0 && s >= 0) bad = true;
+      if (q >= 0 && s >= 0 && q > s) bad = true;
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    if (t == 0) {
+      atomicOr(p.status, GH_DEV_BAD_SEQ);
+      p.loss[0] = __int_as_float(0x7fc00000);
+    }
+    for (int i = t; i < p.N; i += blockDim.x) p.coef[i] = 0.f;
+    return;
+  }
+  if (t == 0) {
+    // first index of the -1 tail (predicate seg < 0 is monotone after the check)
+    int lo_i = 0, hi_i = p.N;
+    while (lo_i < hi_i) {
+      const int mid = (lo_i + hi_i) >> 1;
+      if (p.seg_id[mid] >= 0)
+        lo_i = mid + 1;
+      else
+        hi_i = mid;
+    }
+    s_nvalid = lo_i;
+  }
+  __syncthreads();
+  const int nvalid = s_nvalid;
+
+  // phase 1: warp per segment: S_s, n_s -> rho_s, l_s, per-token gradient
+  bool nonfinite = false;
+  for (int s = warp; s < p.num_segments; s += nw) {
+    const int b = lower_bound_i(p.seg_id, 0, nvalid, s);
+    const int e = lower_bound_i(p.seg_id, b, nvalid, s + 1);
+    float acc = 0.f;
+    int cnt = 0;
+    for (int i = b + lane; i < e; i += 32) {
+      if (!p.mask[i]) continue;
+      acc += p.logp[i] - p.old_logp[i];
+      cnt += 1;
+    }
+    acc = wsum(acc);
+    cnt = wsum_i(cnt);
+    if (lane == 0) {
+      float rho = 1.f, ell = 0.f, g = 0.f;
+      if (cnt > 0) {
+        const float A = p.seg_adv[s];
+        rho = expf(acc / static_cast<float>(cnt));
+        const float c = fminf(fmaxf(rho, lo), hi);
+        ell = -fminf(rho * A, c * A);
+        const bool act = A >= 0.f ? (rho <= hi) : (rho >= lo);
+        const float omega = p.token_weighted ? static_cast<float>(cnt) : 1.f;
+        ell = ell * omega * inv_div;
+        g = act ? (omega * inv_div) * (-A * rho) / static_cast<float>(cnt) : 0.f;
+        if (!isfinite(rho) || !isfinite(ell)) nonfinite = true;
+      }
+      sL[s] = ell;
+      sG[s] = g;
+      if (p.seg_ratio) p.seg_ratio[s] = rho;
+    }
+  }
+  if (nonfinite) atomicOr(p.status, GH_DEV_NONFINITE);
+
+  // mean active logp: per-thread strided sums, then a fixed tree
+  float lps = 0.f;
+  int lpn = 0;
+  for (int i = t; i < p.N; i += blockDim.x)
+    if (p.mask[i]) {
+      lps += p.logp[i];
+      lpn += 1;
+    }
+  lps = wsum(lps);
+  lpn = wsum_i(lpn);
+  if (lane == 0) {
+    red_a[warp] = lps;
+    red_b[warp] = __int_as_float(lpn);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float a = lane < nw ? red_a[lane] : 0.f;
+    int n = lane < nw ? __float_as_int(red_b[lane]) : 0;
+    a = wsum(a);
+    n = wsum_i(n);
+    float L = 0.f;
+    for (int s = lane; s < p.num_segments; s += 32) L += sL[s];
+    L = wsum(L);
+    if (lane == 0) {
+      p.loss[0] = L;
+      if (p.mean_logp) p.mean_logp[0] = n > 0 ? a / static_cast<float>(n) : 0.f;
+    }
+  }
+  // phase 2: coef
+  for (int i = t; i < p.N; i += blockDim.x) {
+    const int s = p.seg_id[i];
+    p.coef[i] = (s >= 0 && p.mask[i]) ? sG[s] : 0.f;
+  }
+}
+
+// ---------------------------------------------------------------- advantages
+__global__ void advantage_kernel(const float* rewards, int num_seqs, int group_size, float eps, float* adv) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  const int groups = num_seqs / group_size;
+  if (g >= groups) return;
+  const float* r = rewards + static_cast<size_t>(g) * group_size;
+  double mean = 0.0;
+  for (int k = 0; k < group_size; ++k) mean += r[k];
+  mean /= group_size;
+  double var = 0.0;
+  for (int k = 0; k < group_size; ++k) var += (r[k] - mean) * (r[k] - mean);
+  const double sd = group_size > 1 ? sqrt(var / (group_size - 1)) : 0.0;
+  for (int k = 0; k < group_size; ++k)
+    adv[static_cast<size_t>(g) * group_size + k] = static_cast<float>((r[k] - mean) / (sd + eps));
+}
+
+// ---------------------------------------------------------------- timeout probe
+__global__ void timeout_probe_kernel(int* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing arrives on `bar`: the bounded wait must give up and report it
+    mbar_wait_bounded(&bar, 0, &abort_flag, status, GH_DEV_TIMEOUT, timeout_ns);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const float* part_s, const float* zy,
+                         const int32_t* targets, const uint8_t* mask, float* logp, float* lse, int* status,
+                         cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  merge_kernel<<<static_cast<unsigned>(ceil_div(N, 256)), 256, 0, st>>>(N, V, splits, part_m, part_s, zy, targets,
+                                                                         mask, logp, lse, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_grpo* g, float* coef, float* loss3,
+                        int* status, cudaStream_t st) {
+  GrpoP p;
+  p.N = N;
+  p.logp = logp;
+  p.old_logp = g->old_logp;
+  p.ref_logp = g->ref_logp;
+  p.adv = g->adv;
+  p.seq_id = g->seq_id;
+  p.mask = mask;
+  p.num_seqs = g->num_seqs;
+  p.reduction = g->reduction;
+  p.eps_low = g->eps_low;
+  p.eps_high = g->eps_high;
+  p.beta = g->beta;
+  p.norm = g->norm;
+  p.coef = coef;
+  p.loss3 = loss3;
+  p.status = status;
+  const size_t sm = static_cast<size_t>(3) * g->num_seqs * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(grpo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         3 * MAX_SEQS * static_cast<int>(sizeof(float)));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  grpo_kernel<<<1, 1024, sm, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gspo(int N, const float* logp, const float* old_logp, const uint8_t* mask, const int32_t* seg_id,
+                        int num_segments, const float* seg_adv, float eps_low, float eps_high, double divisor,
+                        int token_weighted, float* loss, float* seg_ratio, float* coef, float* mean_logp,
+                        int* status, cudaStream_t st) {
+  GspoP p;
+  p.N = N;
+  p.logp = logp;
+  p.old_logp = old_logp;
+  p.mask = mask;
+  p.seg_id = seg_id;
+  p.num_segments = num_segments;
+  p.seg_adv = seg_adv;
+  p.eps_low = eps_low;
+  p.eps_high = eps_high;
+  p.divisor = divisor;
+  p.token_weighted = token_weighted;
+  p.loss = loss;
+  p.seg_ratio = seg_ratio;
+  p.coef = coef;
+  p.mean_logp = mean_logp;
+  p.status = status;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gspo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         2 * MAX_SEQS * static_cast<int>(sizeof(float)));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  gspo_kernel<<<1, 1024, static_cast<size_t>(2) * num_segments * sizeof(float), st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_advantage(const float* rewards, int num_seqs, int group_size, float eps, float* adv,
+                             cudaStream_t st) {
+  const int groups = num_seqs / group_size;
+  if (groups <= 0) return cudaSuccess;
+  advantage_kernel<<<static_cast<unsigned>(ceil_div(groups, 128)), 128, 0, st>>>(rewards, num_seqs, group_size, eps,
+                                                                                 adv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_timeout_probe(int* status, uint64_t tmo, cudaStream_t st) {
+  timeout_probe_kernel<<<1, 32, 0, st>>>(status, tmo);
+  return cudaGetLastError();
+}
+
+}  // namespace gh

@@ -1,0 +1,246 @@
+"""Thin torch-facing binding of the C ABI (argument marshalling only).
+
+Every function takes CUDA tensors, allocates its outputs and scratch space
+with torch (device memory is the only thing torch provides here), and calls
+the library entry point of the same name on the current CUDA stream.  All
+arithmetic runs in the library's kernels; there is no CPU or framework
+fallback.
+
+Device-side status: each call returns (or fills) an int32 status tensor; use
+``raise_on_status`` to read it (a host synchronisation) and raise on errors.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import GhGrpo, GhHead
+
+_BF16 = torch.bfloat16
+_F32 = torch.float32
+
+
+def _lib():
+    return _abi.load()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+class _Workspace:
+    """Grow-only scratch buffer per device (reused across calls)."""
+
+    def __init__(self):
+        self._buf = {}
+
+    def get(self, dev: torch.device, nbytes: int) -> torch.Tensor:
+        key = (dev.type, dev.index)
+        b = self._buf.get(key)
+        if b is None or b.numel() < nbytes:
+            b = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+            self._buf[key] = b
+        return b
+
+    def clear(self):
+        self._buf.clear()
+
+
+WORKSPACE = _Workspace()
+
+
+def make_head(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, mask: torch.Tensor,
+              row_tile: int = 0) -> GhHead:
+    _need(H, "H")
+    _need(W, "W", dtype=H.dtype)
+    if H.dtype not in (_BF16, _F32):
+        raise TypeError("H/W must be bfloat16 or float32")
+    if H.dim() != 2 or W.dim() != 2 or H.shape[1] != W.shape[1]:
+        raise ValueError("H must be [N, D] and W [V, D]")
+    N, D = H.shape
+    V = W.shape[0]
+    _need(targets, "targets", dtype=torch.int32, shape=(N,))
+    _need(mask, "mask", dtype=torch.uint8, shape=(N,))
+    return GhHead(N=N, D=D, V=V, dtype=_abi.GH_BF16 if H.dtype == _BF16 else _abi.GH_FP32, row_tile=row_tile,
+                  H=H.data_ptr(), W=W.data_ptr(), targets=targets.data_ptr(), mask=mask.data_ptr())
+
+
+def forward_workspace_bytes(head: GhHead) -> int:
+    return int(_lib().grpo_head_forward_workspace_size(ctypes.byref(head)))
+
+
+def backward_workspace_bytes(head: GhHead) -> int:
+    return int(_lib().grpo_head_backward_workspace_size(ctypes.byref(head)))
+
+
+def new_status(dev) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=dev)
+
+
+def raise_on_status(status: torch.Tensor, allow: int = 0) -> int:
+    """Read the device status word (synchronises) and raise on any bit not in ``allow``."""
+    word = int(status.item())
+    if word & ~allow:
+        raise _abi.GhError(f"device status {word:#x} ({_abi.describe_status(word)})")
+    return word
+
+
+def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=None, seq_id=None,
+                      num_seqs: int = 0, eps_low: float = 0.2, eps_high: float = 0.2, beta: float = 0.0,
+                      reduction: str = "token_mean", norm: float = 0.0, row_tile: int = 0,
+                      want_coef: bool = True, status: Optional[torch.Tensor] = None, out: Optional[dict] = None):
+    """Selected-token log-probs and LSE; with ``old_logp`` given, also the GRPO
+    loss (loss, policy_loss, kl) and coef = d loss / d logp.
+
+    Returns a dict with logp, lse, and (GRPO) coef, loss3, plus status."""
+    head = make_head(H, W, targets, mask, row_tile)
+    dev = H.device
+    N = head.N
+    out = {} if out is None else out
+    logp = out.get("logp") if out.get("logp") is not None else torch.empty(N, dtype=_F32, device=dev)
+    lse = out.get("lse") if out.get("lse") is not None else torch.empty(N, dtype=_F32, device=dev)
+    st = new_status(dev) if status is None else status
+    g = None
+    coef = loss3 = None
+    if old_logp is not None:
+        _need(old_logp, "old_logp", _F32, (N,))
+        if ref_logp is not None:
+            _need(ref_logp, "ref_logp", _F32, (N,))
+        _need(adv, "adv", _F32)
+        _need(seq_id, "seq_id", torch.int32, (N,))
+        num_seqs = int(num_seqs or adv.numel())
+        g = GhGrpo(old_logp=old_logp.data_ptr(), ref_logp=ref_logp.data_ptr() if ref_logp is not None else None,
+                   adv=adv.data_ptr(), seq_id=seq_id.data_ptr(), num_seqs=num_seqs,
+                   reduction=_abi.REDUCTIONS[reduction], eps_low=eps_low, eps_high=eps_high, beta=beta,
+                   reserved=0.0, norm=float(norm))
+        if want_coef:
+            coef = out.get("coef") if out.get("coef") is not None else torch.empty(N, dtype=_F32, device=dev)
+        loss3 = out.get("loss3") if out.get("loss3") is not None else torch.empty(3, dtype=_F32, device=dev)
+    nbytes = forward_workspace_bytes(head)
+    ws = WORKSPACE.get(dev, nbytes)
+    code = _lib().grpo_head_forward(ctypes.byref(head), ctypes.byref(g) if g is not None else None, _ptr(logp),
+                                    _ptr(lse), _ptr(coef), _ptr(loss3), _ptr(st), _ptr(ws), nbytes, _stream(dev))
+    _abi.check(code, "grpo_head_forward")
+    out.update(logp=logp, lse=lse, coef=coef, loss3=loss3, status=st)
+    return out
+
+
+def gspo_segment_loss(logp, old_logp, mask, seg_id, num_segments: int, seg_adv, *, eps_low: float,
+                      eps_high: float, divisor: float, token_weighted: bool = False,
+                      status: Optional[torch.Tensor] = None):
+    """GSPO sequence-level loss over packed documents; returns loss [1],
+    seg_ratio [S], coef [N], mean_logp [1] and status."""
+    N = logp.numel()
+    _need(logp, "logp", _F32, (N,))
+    _need(old_logp, "old_logp", _F32, (N,))
+    _need(mask, "mask", torch.uint8, (N,))
+    _need(seg_id, "seg_id", torch.int32, (N,))
+    _need(seg_adv, "seg_adv", _F32, (num_segments,))
+    dev = logp.device
+    loss = torch.empty(1, dtype=_F32, device=dev)
+    ratio = torch.empty(num_segments, dtype=_F32, device=dev)
+    coef = torch.empty(N, dtype=_F32, device=dev)
+    mean_logp = torch.empty(1, dtype=_F32, device=dev)
+    st = new_status(dev) if status is None else status
+    code = _lib().gspo_segment_loss(N, _ptr(logp), _ptr(old_logp), _ptr(mask), _ptr(seg_id), num_segments,
+                                    _ptr(seg_adv), eps_low, eps_high, float(divisor), 1 if token_weighted else 0,
+                                    _ptr(loss), _ptr(ratio), _ptr(coef), _ptr(mean_logp), _ptr(st), _stream(dev))
+    _abi.check(code, "gspo_segment_loss")
+    return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, status=st)
+
+
+def grpo_head_backward(H, W, targets, mask, lse, coef, *, grad_out=None, dH=None, dW=None,
+                       accumulate_dW: bool = False, row_tile: int = 0, status: Optional[torch.Tensor] = None):
+    """dH [N, D] (dtype of H) and dW [V, D] fp32 from each row's LSE and coef."""
+    head = make_head(H, W, targets, mask, row_tile)
+    dev = H.device
+    N, D, V = head.N, head.D, head.V
+    _need(lse, "lse", _F32, (N,))
+    _need(coef, "coef", _F32, (N,))
+    if grad_out is not None:
+        _need(grad_out, "grad_out", _F32)
+    if dH is None:
+        dH = torch.empty(N, D, dtype=H.dtype, device=dev)
+    else:
+        _need(dH, "dH", H.dtype, (N, D))
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs an existing dW")
+        dW = torch.empty(V, D, dtype=_F32, device=dev)
+    else:
+        _need(dW, "dW", _F32, (V, D))
+    st = new_status(dev) if status is None else status
+    nbytes = backward_workspace_bytes(head)
+    ws = WORKSPACE.get(dev, nbytes)
+    code = _lib().grpo_head_backward(ctypes.byref(head), _ptr(lse), _ptr(coef), _ptr(grad_out), _ptr(dH), _ptr(dW),
+                                     1 if accumulate_dW else 0, _ptr(st), _ptr(ws), nbytes, _stream(dev))
+    _abi.check(code, "grpo_head_backward")
+    return dict(dH=dH, dW=dW, status=st)
+
+
+def grpo_group_advantage(rewards, group_size: int, eps: float = 1e-4, status: Optional[torch.Tensor] = None):
+    """Group-normalised advantages of per-sequence rewards."""
+    _need(rewards, "rewards", _F32)
+    n = rewards.numel()
+    dev = rewards.device
+    adv = torch.empty(n, dtype=_F32, device=dev)
+    st = new_status(dev) if status is None else status
+    code = _lib().grpo_group_advantage(_ptr(rewards), n, int(group_size), float(eps), _ptr(adv), _ptr(st),
+                                       _stream(dev))
+    _abi.check(code, "grpo_group_advantage")
+    return adv
+
+
+def timeout_probe(timeout_ns: int, dev=None):
+    """Run the bounded-wait self-test; returns the status word (synchronises)."""
+    dev = torch.device("cuda") if dev is None else dev
+    st = new_status(dev)
+    _abi.check(_lib().gh_timeout_probe(_ptr(st), int(timeout_ns), _stream(dev)), "gh_timeout_probe")
+    return int(st.item())
+
+
+# ------------------------------------------------------------------ instrumentation
+def profile_enable(on: bool = True):
+    _lib().gh_profile_enable(1 if on else 0)
+
+
+def profile_reset():
+    _lib().gh_profile_reset()
+
+
+def profile_read():
+    """{kernel name: (launches, total_ms)} since the last reset (synchronises)."""
+    lib = _lib()
+    res = {}
+    for k in range(_abi.NUM_KERNEL_KINDS):
+        n = ctypes.c_int64()
+        ms = ctypes.c_double()
+        _abi.check(lib.gh_profile_read(k, ctypes.byref(n), ctypes.byref(ms)), "gh_profile_read")
+        if n.value:
+            res[lib.gh_kernel_kind_name(k).decode()] = (int(n.value), float(ms.value))
+    return res
+
+
+def launch_count() -> int:
+    return int(_lib().gh_launch_count())

@@ -1,0 +1,208 @@
+/*
+ * grpo_head.h -- C ABI of the fused LM-head GRPO / GSPO loss for GB300 (sm_103a).
+ *
+ * The library computes, from hidden states H[N,D] and the LM-head weight
+ * W[V,D], each token's selected-token log-probability
+ *     logp_i = z_{i,y_i} - LSE_i,   z = H W^T,   LSE_i = log sum_{j<V} exp(z_ij)
+ * by streaming the vocabulary in 256-column tiles (never materialising the
+ * [N,V] logits), the GRPO clipped-ratio + k3-KL loss and its GSPO
+ * sequence-level variant on top, and the backward dH = G W, dW = G^T H with
+ * G = dloss/dz recomputed tile by tile.
+ *
+ * Sources: Liger-Kernel PR #1160 "[GRPO] add chunked grpo streaming over vocab"
+ * (Summary: selected-token log-probs by streaming over vocab, fused-linear
+ * API); RL-Kernel PR #291 "[WS2][PR5][Logp] Add deterministic DP-aware GRPO
+ * loss on the TP-aware logprob path" (PR description: fp32 (max, sumexp)
+ * merge in fixed tile order, padded columns at -inf, (-inf, 0) identity
+ * partial, fp32 logp and LSE outputs, explicit active mask; Key Changes: token
+ * normalisers, per-sequence totals then scalar, (loss, policy_loss, kl));
+ * Fast-LLM PR #554 "Fuse the GSPO segment seam into compiled blocks (#507)"
+ * (What: per-token weights -> index_add_ into segments -> per-segment loss,
+ * new_logprobs metric and per-token backward coefficient; divisor and
+ * grad_output applied outside).
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    never allocates, frees or keeps device memory between calls (scratch
+ *    space is the caller's `ws` buffer, sized by the *_workspace_size calls).
+ *  - All work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream).  Nothing synchronises.
+ *  - The return value reports argument and launch errors (gh_status); a
+ *    message for the last error of the calling thread is in gh_last_error().
+ *  - Data-dependent problems are OR-ed into the caller's device word
+ *    `int32_t *status` (GH_DEV_* bits) without a host synchronisation; the
+ *    caller reads it when it chooses.  `status` must be zeroed by the caller.
+ *  - Row-major layouts; 16-byte aligned base pointers; bf16 rows need
+ *    D % 8 == 0, fp32 rows D % 4 == 0.
+ *  - Results are deterministic (no floating-point atomics) and logp/LSE are
+ *    bitwise independent of row_tile and of the other rows in the batch.
+ */
+#ifndef GRPO_HEAD_H_
+#define GRPO_HEAD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host-side status */
+typedef enum {
+  GH_OK = 0,
+  GH_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or enum is invalid */
+  GH_ERR_UNSUPPORTED = 2, /* valid but not built (e.g. no sm_103a device)  */
+  GH_ERR_WORKSPACE = 3,   /* ws is NULL or smaller than *_workspace_size   */
+  GH_ERR_CUDA = 4         /* a CUDA runtime/driver call failed             */
+} gh_status;
+
+/* device-side status bits OR-ed into *status */
+enum {
+  GH_DEV_TARGET_OOR = 1,  /* an active token's target is outside [0,V); its logp is NaN */
+  GH_DEV_NONFINITE = 2,   /* a non-finite LSE/logp/loss term was produced              */
+  GH_DEV_TIMEOUT = 4,     /* a bounded pipeline wait gave up; outputs are incomplete   */
+  GH_DEV_NO_ACTIVE = 8,   /* token/sequence mean with no active token: loss 0, coef 0  */
+  GH_DEV_BAD_SEQ = 16     /* seq_id/seg_id out of range or not laid out as documented  */
+};
+
+typedef enum { GH_BF16 = 0, GH_FP32 = 1 } gh_dtype;
+
+/* token normalisers (RL-Kernel PR #291, Key Changes: Loss Contract) */
+typedef enum {
+  GH_TOKEN_MEAN = 0, /* w_i = m_i / T, T = active tokens (or `norm` if > 0)            */
+  GH_SEQ_MEAN = 1,   /* w_i = m_i / (n_s L), L = live sequences (or `norm` if > 0)     */
+  GH_FIXED = 2       /* w_i = m_i / C, C = `norm` (> 0), Dr.GRPO constant              */
+} gh_reduction;
+
+/* The LM-head problem shared by forward and backward. */
+typedef struct {
+  int64_t N;              /* tokens (rows of H)                                          */
+  int64_t D;              /* hidden size                                                 */
+  int64_t V;              /* real vocabulary size; padding to 256 columns is internal     */
+  int32_t dtype;          /* gh_dtype of H, W and dH: bf16 (fp32 accumulate, tensor
+                             cores) or fp32 (exact fp32 FMA, no TF32)                    */
+  int32_t row_tile;       /* 0 = default (128) | 64 | 128 | 256: rows per work unit; the
+                             results do not depend on it (bitwise)                       */
+  const void* H;          /* [N, D] row-major                                            */
+  const void* W;          /* [V, D] row-major                                            */
+  const int32_t* targets; /* [N] selected token ids y_i                                  */
+  const uint8_t* mask;    /* [N] 1 = active token; authoritative (inactive targets may
+                             hold any value; inactive rows still get an LSE)             */
+} gh_head;
+
+/* GRPO loss parameters (RL-Kernel PR #291, Overview / Key Changes). */
+typedef struct {
+  const float* old_logp;  /* [N] behaviour-policy log-probs                               */
+  const float* ref_logp;  /* [N] reference-policy log-probs; NULL allowed iff beta == 0   */
+  const float* adv;       /* [num_seqs] per-sequence advantage A_s                        */
+  const int32_t* seq_id;  /* [N] sequence of each token, nondecreasing, in [0, num_seqs)  */
+  int32_t num_seqs;
+  int32_t reduction;      /* gh_reduction                                                 */
+  float eps_low;          /* ratio clipped to [1 - eps_low, 1 + eps_high]                 */
+  float eps_high;
+  float beta;             /* weight of the k3 KL term exp(d) - d - 1, d = ref - logp      */
+  float reserved;         /* must be 0                                                    */
+  double norm;            /* > 0: explicit normaliser (T, L or C above, e.g. the active
+                             token count of the whole step across micro-batches); 0: from
+                             this call (token/seq mean only)                             */
+} gh_grpo;
+
+/* Bytes of scratch `ws` grpo_head_forward needs for this problem. */
+size_t grpo_head_forward_workspace_size(const gh_head* head);
+/* Bytes of scratch `ws` grpo_head_backward needs for this problem. */
+size_t grpo_head_backward_workspace_size(const gh_head* head);
+
+/*
+ * Forward: selected-token log-prob and LSE for every row, and, when `grpo` is
+ * not NULL, the GRPO loss and d loss / d logp.
+ *   logp  [N] fp32 out: z_{i,y_i} - LSE_i (NaN for an active token with an
+ *         out-of-range target, 0 for an inactive one).
+ *   lse   [N] fp32 out: LSE_i over the real vocabulary.
+ *   coef  [N] fp32 out (may be NULL; needs grpo): coef_i = d loss / d logp_i =
+ *         w_i (-A_s r_i act_i + beta (1 - exp(ref_i - logp_i))), with
+ *         r = exp(logp - old), act = 1 where the unclipped PPO term is the min.
+ *   loss3 [3] fp32 out (may be NULL; needs grpo): (loss, policy_loss, kl) with
+ *         loss = policy_loss + beta kl, summed per sequence first and then over
+ *         sequences in index order.
+ * Errors: GH_ERR_INVALID_ARG for bad sizes/pointers/alignment/enums,
+ * GH_ERR_WORKSPACE for a short ws, GH_ERR_CUDA for a failed launch.
+ */
+gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* logp, float* lse,
+                            float* coef, float* loss3, int32_t* status, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/*
+ * GSPO sequence-level loss over packed documents (Fast-LLM PR #554, What):
+ *   S_s = sum_{i in s} m_i (logp_i - old_i), n_s = sum_{i in s} m_i,
+ *   rho_s = exp(S_s / n_s), l_s = -min(rho_s A_s, clip(rho_s) A_s),
+ *   loss = sum_s omega_s l_s / divisor, omega_s = 1 (or n_s if token_weighted),
+ *   coef_i = (omega_s / divisor) (-A_s rho_s act_s) m_i / n_s.
+ * seg_id [N]: document of each token; ids >= 0 are nondecreasing and -1 marks
+ * an unused tail (whose mask must be 0).  Segments with n_s = 0 contribute 0
+ * and report seg_ratio 1.  Outputs: loss [1], seg_ratio [num_segments],
+ * coef [N], mean_logp [1] (the new_logprobs metric: mean active logp); any of
+ * seg_ratio / mean_logp may be NULL.  No scratch memory is needed.
+ */
+gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp, const uint8_t* mask,
+                            const int32_t* seg_id, int32_t num_segments, const float* seg_adv,
+                            float eps_low, float eps_high, double divisor, int32_t token_weighted,
+                            float* loss, float* seg_ratio, float* coef, float* mean_logp,
+                            int32_t* status, void* stream);
+
+/*
+ * Backward of the head given each row's LSE and coef (from grpo_head_forward
+ * or gspo_segment_loss): per vocabulary block the logits are recomputed,
+ *   G_ij = g coef_i (1[j = y_i] - exp(z_ij - LSE_i))   (g = *grad_out, or 1 if NULL)
+ * and dH = G W (fp32 accumulation over blocks in increasing vocabulary order,
+ * written in `dtype`), dW = G^T H (fp32; added to dW when accumulate_dW != 0,
+ * e.g. across micro-batches).  dH [N, D] in dtype; dW [V, D] fp32.
+ */
+gh_status grpo_head_backward(const gh_head* head, const float* lse, const float* coef,
+                             const float* grad_out, void* dH, float* dW, int32_t accumulate_dW,
+                             int32_t* status, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Group-normalised advantages (RL-Kernel PR #291, Reference Op: group-relative
+ * advantage from gathered rewards; review note: two-pass variance):
+ * A = (r - mean_g) / (std_g + eps) over consecutive groups of group_size
+ * sequences, std unbiased (n - 1), 0 for a group of one.  rewards, adv:
+ * [num_seqs] fp32; num_seqs must be a multiple of group_size.
+ */
+gh_status grpo_group_advantage(const float* rewards, int32_t num_seqs, int32_t group_size, float eps,
+                               float* adv, int32_t* status, void* stream);
+
+/* Human-readable name of a gh_status. */
+const char* gh_status_string(gh_status s);
+/* Message of the last error returned on the calling thread ("" if none). */
+const char* gh_last_error(void);
+/* ABI version (major * 100 + minor). */
+int32_t gh_abi_version(void);
+
+/*
+ * Instrumentation (used by the benchmark; off by default).  When enabled, each
+ * kernel the library launches is bracketed by CUDA events on its stream and
+ * counted per kernel kind; gh_profile_read returns, for kind k, the launch
+ * count and the summed event time (ms) since the last reset (it synchronises
+ * the recorded events).  gh_launch_count counts all launches since load.
+ * Kinds: 0 fwd logits+LSE, 1 merge, 2 GRPO loss, 3 GSPO loss, 4 dlogits,
+ * 5 dH GEMM, 6 dW GEMM, 7 advantage, 8 fp32 forward, 9 fp32 dlogits,
+ * 10 fp32 GEMM, 11 timeout probe.
+ */
+#define GH_NUM_KERNEL_KINDS 12
+void gh_profile_enable(int32_t on);
+void gh_profile_reset(void);
+gh_status gh_profile_read(int32_t kind, int64_t* launches, double* total_ms);
+int64_t gh_launch_count(void);
+const char* gh_kernel_kind_name(int32_t kind);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nothing will complete, with a limit of timeout_ns; the wait gives
+ * up, sets GH_DEV_TIMEOUT in *status and the kernel returns normally.
+ */
+gh_status gh_timeout_probe(int32_t* status, uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GRPO_HEAD_H_ */

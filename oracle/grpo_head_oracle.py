@@ -259,8 +259,9 @@ def grpo_loss(logp, old, ref, mask, seq_id, adv, num_seqs: int, eps_low: float,
     w = m * seq_scale[seq]
     coef = w * (-A_tok * r * act + beta * (1.0 - np.exp(d)))
     coef = np.where(m > 0, coef, 0.0)
+    abs_terms = float(np.sum(np.abs(w * (pg + beta * kl))))
     return dict(loss=loss, policy=policy, kl=klsum, coef=coef, per_seq_policy=P,
-                per_seq_kl=K, counts=n, weights=w, ratio=r, act=act)
+                per_seq_kl=K, counts=n, weights=w, ratio=r, act=act, abs_terms=abs_terms)
 
 
 # --------------------------------------------------------------------------
@@ -316,8 +317,10 @@ def gspo_loss(logp, old, mask, seg_id, num_segments: int, seg_adv, eps_low: floa
         if mask[i] and s >= 0:
             coef[i] = g[s] / n[s]
     mean_logp = lp_sum / act_tokens if act_tokens > 0 else 0.0
+    omega_all = n.astype(np.float64) if token_weighted else np.ones(num_segments)
+    abs_terms = float(np.sum(np.abs(omega_all * ell)) / divisor)
     return dict(loss=loss, seg_ratio=rho, seg_loss=ell, coef=coef, counts=n,
-                seg_sum=S, mean_logp=mean_logp)
+                seg_sum=S, mean_logp=mean_logp, abs_terms=abs_terms)
 
 
 # --------------------------------------------------------------------------

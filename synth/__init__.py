@@ -17,7 +17,6 @@ from .workloads import (  # noqa: F401
     bf16_bits_to_f32,
     draw_gspo_layout,
     draw_grpo_layout,
-    draw_head,
     draw_noise,
     draw_rewards,
     f32_to_bf16_bits,

@@ -15,6 +15,7 @@ no public dataset; all values are synthetic.
 from __future__ import annotations
 
 import dataclasses
+import os
 from typing import Optional
 
 import numpy as np
@@ -114,31 +115,64 @@ CONFIGS = (
 )
 
 
+MAX_MICRO_BATCHES = 1024
+CHUNK_ROWS = 2048
+
+
 def _streams(seed: int):
-    """Independent child generators: head weight, layout, rewards, noise, then micro-batches."""
-    ss = np.random.SeedSequence(seed)
-    kids = ss.spawn(4 + 64)
-    return [np.random.Generator(np.random.PCG64(k)) for k in kids]
+    """Independent child seed sequences: head weight, layout, rewards, noise,
+    then one per micro-batch."""
+    return np.random.SeedSequence(seed).spawn(4 + MAX_MICRO_BATCHES)
+
+
+def _gen(ss):
+    return np.random.Generator(np.random.PCG64(ss))
+
+
+def _normal_rows(ss, rows: int, cols: int, std: float) -> np.ndarray:
+    """N(0, std^2) float32 [rows, cols]; row chunks of CHUNK_ROWS come from their
+    own child streams and are drawn in parallel threads, so the values do not
+    depend on the thread count."""
+    out = np.empty((rows, cols), dtype=np.float32)
+    nchunk = (rows + CHUNK_ROWS - 1) // CHUNK_ROWS
+    kids = ss.spawn(nchunk)
+
+    def fill(c):
+        r0 = c * CHUNK_ROWS
+        r1 = min(rows, r0 + CHUNK_ROWS)
+        _gen(kids[c]).standard_normal((r1 - r0, cols), dtype=np.float32, out=out[r0:r1])
+        if std != 1.0:
+            out[r0:r1] *= np.float32(std)
+
+    if nchunk == 1:
+        fill(0)
+    else:
+        import concurrent.futures as cf
+        with cf.ThreadPoolExecutor(max_workers=min(nchunk, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(nchunk)))
+    return out
+
+
+def _bf16_rows(x: np.ndarray) -> np.ndarray:
+    """f32_to_bf16_bits applied chunk-wise in parallel threads."""
+    out = np.empty(x.shape, dtype=np.uint16)
+    n = x.shape[0]
+    if n <= CHUNK_ROWS:
+        out[...] = f32_to_bf16_bits(x)
+        return out
+    import concurrent.futures as cf
+
+    def conv(r0):
+        out[r0:r0 + CHUNK_ROWS] = f32_to_bf16_bits(x[r0:r0 + CHUNK_ROWS])
+
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        list(ex.map(conv, range(0, n, CHUNK_ROWS)))
+    return out
 
 
 # --------------------------------------------------------------------------
 # raw draws
 # --------------------------------------------------------------------------
-def draw_head(rng_w, rng_h, N: int, D: int, V: int, w_std: float, dtype: str):
-    """H ~ N(0,1) [N,D]; W ~ N(0, w_std^2) [V,D]; targets ~ U[0,V) [N].
-
-    fp32: float32 arrays.  bf16: uint16 bit arrays (rounded from float32)."""
-    W = rng_w.standard_normal((V, D), dtype=np.float32)
-    W *= np.float32(w_std)
-    H = rng_h.standard_normal((N, D), dtype=np.float32)
-    y = rng_h.integers(0, V, size=N, dtype=np.int64).astype(np.int32)
-    if dtype == "bf16":
-        return f32_to_bf16_bits(H), f32_to_bf16_bits(W), y
-    if dtype == "fp32":
-        return H, W, y
-    raise ValueError(dtype)
-
-
 def draw_grpo_layout(rng, num_seqs: int, seq_len: int, len_lo: int, len_hi: int):
     """Padded GRPO layout: sequence s owns tokens [s*T, (s+1)*T); its first
     L_s ~ U[len_lo, len_hi] (inclusive) tokens are the active completion."""
@@ -194,22 +228,24 @@ def make_workload(cfg: WorkloadConfig, micro_batch: int = 0, *, N: Optional[int]
     GRPO layout then keeps whole sequences), ``dtype`` the storage type.
     W does not depend on ``micro_batch`` or ``N``; ``with_weight=False``
     skips drawing it (the caller already holds it)."""
+    if not 0 <= micro_batch < MAX_MICRO_BATCHES:
+        raise ValueError("micro_batch out of range")
     st = _streams(cfg.seed)
-    rng_w, rng_layout, rng_rew, rng_noise = st[0], st[1], st[2], st[3]
-    rng_mb = st[4 + micro_batch]
+    rng_layout, rng_rew, rng_noise = _gen(st[1]), _gen(st[2]), _gen(st[3])
+    ss_mb = st[4 + micro_batch]
+    ss_h, ss_y = ss_mb.spawn(2)
     dt = dtype or cfg.dtype
     n_tok = N if N is not None else cfg.N
     out = dict(cfg=cfg, N=n_tok, D=cfg.D, V=cfg.V, dtype=dt,
                eps_low=cfg.eps_low, eps_high=cfg.eps_high, beta=cfg.beta)
 
     if with_weight:
-        W = rng_w.standard_normal((cfg.V, cfg.D), dtype=np.float32)
-        W *= np.float32(cfg.weight_std())
-        out["W"] = f32_to_bf16_bits(W) if dt == "bf16" else W
+        W = _normal_rows(st[0], cfg.V, cfg.D, cfg.weight_std())
+        out["W"] = _bf16_rows(W) if dt == "bf16" else W
         del W
-    H = rng_mb.standard_normal((n_tok, cfg.D), dtype=np.float32)
-    out["H"] = f32_to_bf16_bits(H) if dt == "bf16" else H
-    out["targets"] = rng_mb.integers(0, cfg.V, size=n_tok, dtype=np.int64).astype(np.int32)
+    H = _normal_rows(ss_h, n_tok, cfg.D, 1.0)
+    out["H"] = _bf16_rows(H) if dt == "bf16" else H
+    out["targets"] = _gen(ss_y).integers(0, cfg.V, size=n_tok, dtype=np.int64).astype(np.int32)
 
     # the layout streams are advanced micro_batch times so each micro-batch differs
     if cfg.kind == "grpo":

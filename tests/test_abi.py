@@ -1,0 +1,138 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every entry
+point declared in include/grpo_head.h; the ctypes struct layouts match the C
+ones; host-only calls (names, versions, workspace sizes, argument
+validation) behave as documented.  No kernel is launched here."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "grpo_head.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available to build the library")
+    from gspo_logprob_gb300 import build
+    build()
+    from gspo_logprob_gb300 import _abi
+    return _abi.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "grpo_head_forward" in names and "gspo_segment_loss" in names and "grpo_head_backward" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in the header but not exported"
+    from gspo_logprob_gb300 import _abi
+    assert set(names) == set(_abi.SIGNATURES), "ctypes signatures and header declarations differ"
+
+
+def test_struct_layout_matches_c(lib, tmp_path):
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    prog = tmp_path / "layout.c"
+    prog.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "grpo_head.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(gh_head), offsetof(gh_head, H),"
+        " offsetof(gh_head, mask), sizeof(gh_grpo), offsetof(gh_grpo, num_seqs), offsetof(gh_grpo, norm));return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    from gspo_logprob_gb300._abi import GhGrpo, GhHead
+    want = [ctypes.sizeof(GhHead), GhHead.H.offset, GhHead.mask.offset, ctypes.sizeof(GhGrpo),
+            GhGrpo.num_seqs.offset, GhGrpo.norm.offset]
+    assert got == want
+
+
+def test_host_only_calls(lib):
+    assert lib.gh_abi_version() == 100
+    assert lib.gh_status_string(0) == b"GH_OK"
+    assert lib.gh_status_string(3) == b"GH_ERR_WORKSPACE"
+    assert lib.gh_kernel_kind_name(0) == b"fwd_logits_lse_tc"
+    assert lib.gh_kernel_kind_name(99) == b""
+
+
+def _head(N=1000, D=256, V=5000, dtype=0, row_tile=0, aligned=True):
+    from gspo_logprob_gb300._abi import GhHead
+    base = 0x10000 if aligned else 0x10004
+    return GhHead(N=N, D=D, V=V, dtype=dtype, row_tile=row_tile, H=base, W=base, targets=base, mask=base)
+
+
+def test_workspace_sizes(lib):
+    h = _head(N=1000, D=256, V=5000)
+    # forward: two [splits, N] fp32 partial arrays + zy [N]; splits = ceil(ceil(5000/256)/4) = 5
+    fw = lib.grpo_head_forward_workspace_size(ctypes.byref(h))
+    al = lambda x: (x + 255) // 256 * 256
+    assert fw == 2 * al(5 * 1000 * 4) + al(1000 * 4)
+    # backward (bf16): G block of min(5120, 4096) columns, plus the fp32 dH accumulator (2 blocks)
+    bw = lib.grpo_head_backward_workspace_size(ctypes.byref(h))
+    assert bw == al(1000 * 4096 * 2) + al(1000 * 256 * 4)
+    # a single-block vocabulary needs no accumulator
+    h2 = _head(N=64, D=64, V=500)
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h2)) == al(64 * 512 * 2)
+    # invalid problem -> 0
+    assert lib.grpo_head_forward_workspace_size(ctypes.byref(_head(D=12))) == 0
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(D=12), b"D % 8"),
+    (dict(row_tile=96), b"row_tile"),
+    (dict(dtype=7), b"dtype"),
+    (dict(V=0), b"V="),
+    (dict(aligned=False), b"aligned"),
+])
+def test_argument_validation(lib, kw, msg):
+    h = _head(**kw)
+    st = lib.grpo_head_forward(ctypes.byref(h), None, 0x100, 0x100, None, None, 0x100, 0x100, 1 << 30, None)
+    assert st == 1  # GH_ERR_INVALID_ARG
+    assert msg in lib.gh_last_error()
+
+
+def test_workspace_too_small_is_reported(lib):
+    h = _head()
+    st = lib.grpo_head_forward(ctypes.byref(h), None, 0x100, 0x100, None, None, 0x100, 0x100, 16, None)
+    assert st == 3  # GH_ERR_WORKSPACE
+
+
+def test_no_gpu_fails_loudly(lib):
+    # with a valid problem but no sm_103 device the call must refuse, not fall back
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    h = _head()
+    st = lib.grpo_head_forward(ctypes.byref(h), None, 0x100, 0x100, None, None, 0x100, 0x100, 1 << 30, None)
+    assert st == 2  # GH_ERR_UNSUPPORTED
+    assert b"sm_103" in lib.gh_last_error()
+
+
+def test_gspo_and_advantage_validation(lib):
+    st = lib.gspo_segment_loss(10, 0x100, 0x100, 0x100, 0x100, 0, 0x100, 0.2, 0.2, 1.0, 0, 0x100, None, 0x100,
+                               None, 0x100, None)
+    assert st == 1 and b"num_segments" in lib.gh_last_error()
+    st = lib.gspo_segment_loss(10, 0x100, 0x100, 0x100, 0x100, 4, 0x100, 0.2, 0.2, 0.0, 0, 0x100, None, 0x100,
+                               None, 0x100, None)
+    assert st == 1 and b"divisor" in lib.gh_last_error()
+    st = lib.grpo_group_advantage(0x100, 10, 4, 1e-4, 0x100, 0x100, None)
+    assert st == 1 and b"multiple" in lib.gh_last_error()
+
+
+def test_binding_imports_without_gpu():
+    import gspo_logprob_gb300 as g
+    assert callable(g.grpo_head_forward) and callable(g.grpo_head_backward)

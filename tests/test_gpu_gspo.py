@@ -1,0 +1,128 @@
+"""GPU parity of the GSPO segment seam (kernel alone on seeded log-probs, and
+end to end through the head forward/backward) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import CONFIGS, make_workload
+
+from gpu_helpers import (BF16_LOSS_REL, assert_grad_bf16, bf16_np, dev_head, dev_tensor, gpu_lib,  # noqa: F401
+                         host_head)
+
+pytestmark = pytest.mark.gpu
+
+
+def _seg_adv(w):
+    return oracle.group_advantages(w["rewards"], w["group_size"]).astype(np.float32)
+
+
+@pytest.mark.parametrize("masked_frac,token_weighted", [(0.0, False), (0.1, False), (0.1, True)])
+def test_gspo_kernel_vs_oracle(gpu_lib, masked_frac, token_weighted):
+    import gspo_logprob_gb300 as g
+    cfg = CONFIGS[3]
+    w = make_workload(cfg, masked_frac=masked_frac, with_weight=False, old_noise=0.01)
+    rng = np.random.default_rng(7)
+    N = cfg.N
+    logp = (-rng.uniform(0.05, 6.0, N)).astype(np.float32)       # seeded stand-in log-probs
+    old = (logp.astype(np.float64) + w["u_old"]).astype(np.float32)
+    A = _seg_adv(w)
+    S = cfg.num_docs
+    res = g.gspo_segment_loss(dev_tensor(logp), dev_tensor(old), dev_tensor(w["mask"]), dev_tensor(w["seq_id"]), S,
+                              dev_tensor(A), eps_low=cfg.eps_low, eps_high=cfg.eps_high, divisor=float(S),
+                              token_weighted=token_weighted)
+    o = oracle.gspo_loss(logp.astype(np.float64), old.astype(np.float64), w["mask"], w["seq_id"], S,
+                         A.astype(np.float64), cfg.eps_low, cfg.eps_high, float(S), token_weighted)
+    assert int(res["status"].item()) == 0
+    sc = max(abs(o["loss"]), o["abs_terms"])
+    assert abs(float(res["loss"].item()) - o["loss"]) <= 1e-5 * sc
+    np.testing.assert_allclose(res["seg_ratio"].cpu().numpy(), o["seg_ratio"], rtol=1e-5, atol=0)
+    cg = res["coef"].cpu().numpy()
+    rho = o["seg_ratio"]
+    edge = (np.abs(rho - (1 - cfg.eps_low)) < 1e-6) | (np.abs(rho - (1 + cfg.eps_high)) < 1e-6)
+    ok_tok = np.array([(s < 0) or not edge[s] for s in w["seq_id"]])
+    np.testing.assert_allclose(cg[ok_tok], o["coef"][ok_tok], rtol=1e-4, atol=1e-9)
+    assert abs(float(res["mean_logp"].item()) - o["mean_logp"]) <= 1e-5 * abs(o["mean_logp"])
+    # exact: which tokens carry a coefficient (mask and segment membership)
+    assert np.array_equal(cg != 0, o["coef"] != 0)
+
+
+def test_gspo_end_to_end(gpu_lib):
+    # packed-document layout of the GSPO workload with N cut to 2048 tokens so the
+    # fp64 oracle runs the whole forward/backward in seconds
+    import gspo_logprob_gb300 as g
+    cfg = CONFIGS[3]
+    w = make_workload(cfg, N=2048, masked_frac=0.1)
+    H, W = host_head(w)
+    lp_o, lse_o, _ = oracle.selected_logprob(H, W, w["targets"], w["mask"])
+    old = (lp_o + w["u_old"]).astype(np.float32)
+    A = _seg_adv(w)
+    S = cfg.num_docs
+    o = oracle.gspo_loss(lp_o, old.astype(np.float64), w["mask"], w["seq_id"], S, A.astype(np.float64),
+                         cfg.eps_low, cfg.eps_high, float(S))
+    dH_o, dW_o = oracle.head_backward(H, W, w["targets"], lse_o, o["coef"])
+
+    Hd, Wd, y, m = dev_head(w)
+    fw = g.grpo_head_forward(Hd, Wd, y, m)
+    gs = g.gspo_segment_loss(fw["logp"], dev_tensor(old), m, dev_tensor(w["seq_id"]), S, dev_tensor(A),
+                             eps_low=cfg.eps_low, eps_high=cfg.eps_high, divisor=float(S))
+    bw = g.grpo_head_backward(Hd, Wd, y, m, fw["lse"], gs["coef"])
+    torch.cuda.synchronize()
+    assert int(fw["status"].item()) == 0 and int(gs["status"].item()) == 0 and int(bw["status"].item()) == 0
+    assert np.max(np.abs(fw["logp"].cpu().numpy() - lp_o)) <= 3e-2
+    sc = max(abs(o["loss"]), o["abs_terms"])
+    assert abs(float(gs["loss"].item()) - o["loss"]) <= BF16_LOSS_REL * sc
+    # the tight clip band (3e-4 / 4e-4) puts some segment ratios near an edge,
+    # where the gradient switches on or off: compare only when none is there
+    rho = o["seg_ratio"]
+    near = (np.abs(rho - (1 - cfg.eps_low)) < 2e-5) | (np.abs(rho - (1 + cfg.eps_high)) < 2e-5)
+    if not near.any():
+        assert_grad_bf16(bf16_np(bw["dH"]), dH_o, "dH")
+        assert_grad_bf16(bw["dW"].cpu().numpy(), dW_o, "dW")
+    assert np.array_equal(gs["coef"].cpu().numpy() != 0, o["coef"] != 0) or near.any()
+
+
+def test_gspo_end_to_end_wide_band(gpu_lib):
+    # same pipeline with a wide clip band so every segment carries a gradient
+    import gspo_logprob_gb300 as g
+    cfg = CONFIGS[3]
+    w = make_workload(cfg, N=1536)
+    H, W = host_head(w)
+    lp_o, lse_o, _ = oracle.selected_logprob(H, W, w["targets"], w["mask"])
+    old = (lp_o + w["u_old"]).astype(np.float32)
+    A = _seg_adv(w)
+    S = cfg.num_docs
+    o = oracle.gspo_loss(lp_o, old.astype(np.float64), w["mask"], w["seq_id"], S, A.astype(np.float64), 0.2, 0.2,
+                         float(S))
+    dH_o, dW_o = oracle.head_backward(H, W, w["targets"], lse_o, o["coef"])
+    Hd, Wd, y, m = dev_head(w)
+    fw = g.grpo_head_forward(Hd, Wd, y, m)
+    gs = g.gspo_segment_loss(fw["logp"], dev_tensor(old), m, dev_tensor(w["seq_id"]), S, dev_tensor(A),
+                             eps_low=0.2, eps_high=0.2, divisor=float(S))
+    bw = g.grpo_head_backward(Hd, Wd, y, m, fw["lse"], gs["coef"])
+    sc = max(abs(o["loss"]), o["abs_terms"])
+    assert abs(float(gs["loss"].item()) - o["loss"]) <= BF16_LOSS_REL * sc
+    assert_grad_bf16(bf16_np(bw["dH"]), dH_o, "dH")
+    assert_grad_bf16(bw["dW"].cpu().numpy(), dW_o, "dW")
+
+
+def test_gspo_layout_errors(gpu_lib):
+    import gspo_logprob_gb300 as g
+    N = 64
+    logp = torch.zeros(N, device="cuda")
+    mask = torch.ones(N, dtype=torch.uint8, device="cuda")
+    seg = torch.arange(N, dtype=torch.int32, device="cuda") // 8
+    A = torch.ones(8, device="cuda")
+    ok = g.gspo_segment_loss(logp, logp, mask, seg, 8, A, eps_low=0.2, eps_high=0.2, divisor=8.0)
+    assert int(ok["status"].item()) == 0
+    assert abs(float(ok["loss"].item()) + 1.0) < 1e-6  # ratio 1, A = 1: every segment loss is -1
+    bad = seg.clone()
+    bad[20] = 0  # goes back to an earlier document
+    r = g.gspo_segment_loss(logp, logp, mask, bad, 8, A, eps_low=0.2, eps_high=0.2, divisor=8.0)
+    assert int(r["status"].item()) & 16
+    bad = seg.clone()
+    bad[5] = -1  # an unused slot inside the documents
+    mask2 = mask.clone()
+    mask2[5] = 0
+    r = g.gspo_segment_loss(logp, logp, mask2, bad, 8, A, eps_low=0.2, eps_high=0.2, divisor=8.0)
+    assert int(r["status"].item()) & 16
