@@ -16,7 +16,7 @@ __all__ = ["grpo_head_forward", "gspo_segment_loss", "grpo_head_backward", "grpo
 
 
 def build(verbose: bool = False) -> str:
-    from .build import build as _build
+    from .buildlib import build as _build
     return _build(verbose=verbose)
 
 
