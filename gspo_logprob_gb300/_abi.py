@@ -22,6 +22,7 @@ GH_BF16, GH_FP32 = 0, 1
 GH_TOKEN_MEAN, GH_SEQ_MEAN, GH_FIXED = 0, 1, 2
 REDUCTIONS = {"token_mean": GH_TOKEN_MEAN, "seq_mean": GH_SEQ_MEAN, "fixed": GH_FIXED}
 NUM_KERNEL_KINDS = 12
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # GH_NOALLOC_SCRATCH_BYTES
 
 
 class GhHead(ctypes.Structure):
@@ -47,6 +48,8 @@ SIGNATURES = {
     "grpo_head_backward": (c_int32, [POINTER(GhHead), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                      c_void_p, c_void_p, c_size_t, c_void_p]),
     "grpo_group_advantage": (c_int32, [c_void_p, c_int32, c_int32, c_float, c_void_p, c_void_p, c_void_p]),
+    "grpo_head_forward_noalloc": (c_int32, [POINTER(GhHead), POINTER(GhGrpo), c_void_p, c_void_p, c_void_p,
+                                            c_void_p, c_void_p, c_void_p]),
     "gh_status_string": (c_char_p, [c_int32]),
     "gh_last_error": (c_char_p, []),
     "gh_abi_version": (c_int32, []),

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgrpohead.so")
-SOURCES = ["tc_kernels.cu", "simt_kernels.cu", "loss_kernels.cu", "api.cpp"]
+SOURCES = ["tc_kernels.cu", "simt_kernels.cu", "loss_kernels.cu", "api.cpp", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

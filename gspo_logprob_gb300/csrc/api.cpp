@@ -31,6 +31,8 @@ static gh_status fail(gh_status s, const char* fmt, ...) {
   return s;
 }
 
+void set_error_message(const std::string& msg) { g_last_error = msg; }
+
 static gh_status cuda_fail(cudaError_t e, const char* what) {
   return fail(GH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }

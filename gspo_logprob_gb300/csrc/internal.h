@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <string>
 
 #include "grpo_head.h"
 
@@ -49,6 +50,8 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 
 int num_sms();
 uint64_t timeout_ns();
+// Sets the calling thread's gh_last_error() message.
+void set_error_message(const std::string& msg);
 
 // --- tcgen05 launchers (tc_kernels.cu) ---------------------------------------
 struct TcFwdArgs {

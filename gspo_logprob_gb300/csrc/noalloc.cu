@@ -1,0 +1,86 @@
+// Forward entry point for callers that cannot allocate device memory.
+//
+// grpo_head_forward needs scratch space (per-split LSE partials and the
+// gathered target logits) that the caller normally provides as `ws`.  Some
+// callers cannot provide it: their device memory is entirely owned by another
+// allocator (a framework's caching allocator that has reserved the pool, or a
+// memory plan fixed before the step starts), or they must not call cudaMalloc
+// in the middle of a step because cudaMalloc can synchronise the device.  For
+// them grpo_head_forward_noalloc runs the same forward with its scratch in the
+// fixed device array below, so the caller only passes inputs and outputs.
+//
+// The array is GH_NOALLOC_SCRATCH_BYTES (16 MiB); every GPU that loads this
+// library holds it until the process exits.  Its device address is looked up
+// once per device (with that device current) on the first call made there, so
+// that first call should come before any stream capture.  All calls share the
+// array: calls whose GPU work overlaps (different streams or threads) race on
+// it and must be serialised by the caller.  The array keeps the previous
+// call's contents; nothing in it has to start at zero, because the forward
+// writes every scratch slot it later reads within the same call.
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "grpo_head.h"
+#include "internal.h"
+
+namespace gh {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GH_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device (looked up once).
+gh_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error_message(std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    return GH_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) {
+    set_error_message("device index out of range for the no-allocation scratch table");
+    return GH_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      set_error_message(std::string("cudaGetSymbolAddress(no-allocation scratch): ") + cudaGetErrorString(e));
+      return GH_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return GH_OK;
+}
+
+}  // namespace
+}  // namespace gh
+
+extern "C" gh_status grpo_head_forward_noalloc(const gh_head* head, const gh_grpo* grpo, float* logp, float* lse,
+                                               float* coef, float* loss3, int32_t* status, void* stream) {
+  const size_t need = grpo_head_forward_workspace_size(head);
+  if (need == 0) {
+    // invalid problem (the regular entry point reports why) or one needing no scratch
+    return grpo_head_forward(head, grpo, logp, lse, coef, loss3, status, nullptr, 0, stream);
+  }
+  if (need > static_cast<size_t>(GH_NOALLOC_SCRATCH_BYTES)) {
+    char buf[256];
+    snprintf(buf, sizeof(buf),
+             "problem needs %zu bytes of forward scratch, more than the %zu-byte no-allocation buffer "
+             "(use grpo_head_forward with a caller workspace)",
+             need, static_cast<size_t>(GH_NOALLOC_SCRATCH_BYTES));
+    gh::set_error_message(buf);
+    return GH_ERR_INVALID_ARG;
+  }
+  void* scratch = nullptr;
+  const gh_status s = gh::noalloc_scratch(&scratch);
+  if (s != GH_OK) return s;
+  return grpo_head_forward(head, grpo, logp, lse, coef, loss3, status, scratch,
+                           static_cast<size_t>(GH_NOALLOC_SCRATCH_BYTES), stream);
+}

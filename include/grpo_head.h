@@ -23,8 +23,9 @@
  *
  * Conventions shared by every entry point:
  *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
- *    never allocates, frees or keeps device memory between calls (scratch
- *    space is the caller's `ws` buffer, sized by the *_workspace_size calls).
+ *    never allocates or frees device memory, and keeps none between calls apart
+ *    from the fixed scratch array of grpo_head_forward_noalloc (scratch space is
+ *    otherwise the caller's `ws` buffer, sized by the *_workspace_size calls).
  *  - All work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *    void*; NULL = the legacy default stream).  Nothing synchronises.
  *  - The return value reports argument and launch errors (gh_status); a
@@ -170,6 +171,31 @@ gh_status grpo_head_backward(const gh_head* head, const float* lse, const float*
  */
 gh_status grpo_group_advantage(const float* rewards, int32_t num_seqs, int32_t group_size, float eps,
                                float* adv, int32_t* status, void* stream);
+
+/*
+ * Forward without a caller workspace.  The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory -- their
+ * device memory is wholly owned by another allocator (a framework's caching
+ * allocator that has reserved the pool, or a memory plan fixed before the
+ * step), or they must not call cudaMalloc mid-step because it can synchronise
+ * the device -- and so cannot hand grpo_head_forward its `ws` buffer.
+ *
+ * Same arguments, outputs and results as grpo_head_forward (bitwise), minus
+ * `ws`/`ws_bytes`: the scratch lives in a fixed, file-scope device array of
+ * GH_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until the
+ * process exits.  Nothing is allocated or freed by the call.  A problem whose
+ * forward scratch (grpo_head_forward_workspace_size) exceeds that size is
+ * rejected with GH_ERR_INVALID_ARG and a message in gh_last_error() before
+ * any GPU work.  The array's device address is looked up on the first call
+ * made on each device (with that device current), so make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (nothing in it needs to start at zero): calls whose GPU
+ * work overlaps in time, e.g. on two streams, race on it and must be
+ * serialised by the caller.
+ */
+#define GH_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+gh_status grpo_head_forward_noalloc(const gh_head* head, const gh_grpo* grpo, float* logp, float* lse,
+                                    float* coef, float* loss3, int32_t* status, void* stream);
 
 /* Human-readable name of a gh_status. */
 const char* gh_status_string(gh_status s);
