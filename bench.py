@@ -146,6 +146,24 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(num(r[3]) for r in rows)}
 
 
+def kernel_traffic(name: str):
+    """DRAM bytes per launch of `name` from the committed ncu summary, or None
+    when the kernel sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic_tc_kernels_8b_vocab.json")
+    try:
+        d = json.load(open(path))
+        h = hashlib.sha256()
+        for src in d["source_files"]:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        if h.hexdigest() != d["source_sha256"]:
+            return None
+        k = d["kernels"][name]
+        return int(k["dram_read_bytes"]) + int(k["dram_write_bytes"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -335,7 +353,8 @@ def run_ours(args, rank, world, local):
     dom = max((k for k in kernels if k in alg), key=lambda k: kernels[k]["ms_per_step"])
     dom_launches = kernels[dom]["launches_per_step"]
     roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["tflops"], "peak": sustained,
-            "unit": "TFLOP/s", "frac": round(kernels[dom]["tflops"] / sustained, 4), "traffic": None,
+            "unit": "TFLOP/s", "frac": round(kernels[dom]["tflops"] / sustained, 4), "traffic": kernel_traffic(dom),
+            "traffic_unit": "bytes per launch (ncu dram read+write, one capture; null if the kernel changed)",
             "algorithmic_flops_per_launch": alg[dom] / dom_launches,
             "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a multi-second step)"}
     ws_bytes = max(ops.forward_workspace_bytes(ops.make_head(H[0], W, y[0], m[0])),

@@ -67,6 +67,16 @@ static bool device_is_sm103() {
   return cache[dev] == 1;
 }
 
+int bwd_block_cols() {
+  static int v = 0;
+  if (v == 0) {
+    const char* e = getenv("GH_BWD_BLOCK_COLS");
+    const int x = e ? atoi(e) : 0;
+    v = (x >= VTILE && x % VTILE == 0 && x <= (1 << 20)) ? x : 16384;
+  }
+  return v;
+}
+
 uint64_t timeout_ns() {
   static uint64_t t = 0;
   if (t == 0) {
@@ -208,7 +218,8 @@ struct BwdWs {
 static BwdWs bwd_layout(const gh_head* h, void* base) {
   const int64_t Vp = ceil_div(h->V, VTILE) * VTILE;
   BwdWs w;
-  w.vb = Vp < BWD_BLOCK_COLS ? Vp : BWD_BLOCK_COLS;
+  const int64_t cols = bwd_block_cols();
+  w.vb = Vp < cols ? Vp : cols;
   w.nblk = ceil_div(Vp, w.vb);
   const size_t elt = h->dtype == GH_BF16 ? 2 : 4;
   const size_t g = align_up(static_cast<size_t>(h->N) * w.vb * elt, 256);

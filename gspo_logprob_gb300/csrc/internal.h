@@ -16,8 +16,11 @@ namespace gh {
 constexpr int VTILE = 256;
 constexpr int TILES_PER_SPLIT = 4;
 constexpr int SPLIT_COLS = VTILE * TILES_PER_SPLIT;
-// Backward vocabulary block (columns of dlogits held in the workspace at once).
-constexpr int BWD_BLOCK_COLS = 4096;
+// Backward vocabulary block (columns of dlogits held in the workspace at once):
+// 16384 by default (fewer fp32 dH read-modify-write passes), or a multiple of
+// 256 from GH_BWD_BLOCK_COLS (a tuning knob; dW and the dlogits are the same
+// for any width, dH differs only in the fp32 rounding of its accumulation).
+int bwd_block_cols();
 // Maximum sequences / segments handled by the single-CTA loss kernels.
 constexpr int MAX_SEQS = 16384;
 

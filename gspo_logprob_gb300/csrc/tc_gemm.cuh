@@ -2,14 +2,18 @@
 //
 //   warp 0      : TMA producer (one thread) -- stages bf16 A/B tiles in shared memory
 //   warp 1      : TMEM allocator + MMA issuer (one thread) -- tcgen05.mma M=128 N=256 K=16
-//   warps 2..5  : epilogue (128 threads, thread t owns TMEM lane / tile row t)
+//   warps 2..    : epilogue (4 warps per 128-row block; thread t owns TMEM lane /
+//                  tile row t of its block)
 //
-// The accumulator is double-buffered in TMEM (2 x 256 fp32 columns) so the
-// epilogue of tile i overlaps the MMAs of tile i+1.  Work is a list of tasks;
-// a task is a fixed run of tiles (m_per_task row blocks x n_per_task column
-// blocks, ordered n-major then m) handed to one CTA in order, so an epilogue
-// can carry state across the tiles of a task (the online log-sum-exp of a
-// vocabulary split).  Tasks are dealt round-robin to gridDim.x persistent CTAs.
+// A CTA tile is MT x 128 rows by 256 columns.  With MT = 1 the accumulator is
+// double-buffered in TMEM (2 x 256 fp32 columns) so the epilogue of tile i
+// overlaps the MMAs of tile i+1; with MT = 2 both 128-row blocks multiply the
+// same staged B tile (one B fill per 256 x 256 tile) into the two halves of
+// TMEM.  Work is a list of tasks; a task is one row tile and n_per_task
+// consecutive column blocks handed to one CTA in order, so an epilogue can
+// carry state across the tiles of a task (the online log-sum-exp of a
+// vocabulary split).  Tasks are rastered in groups of group_m row tiles
+// (row fastest) for L2 reuse and dealt round-robin to gridDim.x persistent CTAs.
 //
 // Operand layouts (bf16, 128-byte swizzle, tiles 1024-byte aligned):
 //   K-major A: TMA box {64 (K), 128 rows}; rows at 128 B, 8-row groups at 1024 B.
@@ -29,37 +33,45 @@
 
 namespace gh {
 
-constexpr int TC_BM = 128;
-constexpr int TC_BN = 256;
-constexpr int TC_BK = 64;
-constexpr int TC_STAGES = 4;
-constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
+constexpr int TC_BM = 128;   // rows per tcgen05.mma (TMEM lanes)
+constexpr int TC_BN = 256;   // columns per tile
+constexpr int TC_BK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB per 128-row A block
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 32 KB
-constexpr int TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;
-constexpr int TC_THREADS = 192;
 constexpr int TC_TMEM_COLS = 512;
-constexpr int TC_SMEM_BYTES = TC_STAGES * TC_STAGE_BYTES + 1024 + 256;
 constexpr float LOG2E = 1.4426950408889634f;
 
-struct TcSched {
-  int num_m_blocks;  // row blocks of A (each m_step rows apart, 128 rows loaded)
-  int num_n_blocks;  // 256-wide column blocks
-  int m_per_task;    // 1 or 2
-  int n_per_task;
-  int num_kb;        // 64-deep K blocks
-  int m_step;        // 128, or 64 for half-height row tiles
-  int num_mg;        // ceil(num_m_blocks / m_per_task)
-  int num_tasks;     // num_mg * ceil(num_n_blocks / n_per_task)
+// MT = 128-row MMA blocks per CTA tile (1: 128 x 256 tiles, double-buffered
+// accumulator; 2: 256 x 256 tiles whose two row blocks share every staged B
+// tile -- a third less shared-memory fill traffic per FLOP -- with a single
+// 2 x 256-column accumulator and twice the epilogue warps).
+template <int MT>
+struct TcCfg {
+  static constexpr int STAGE_BYTES = MT * TC_A_BYTES + TC_B_BYTES;
+  static constexpr int STAGES = MT == 1 ? 4 : 3;
+  static constexpr int NUM_ACC = MT == 1 ? 2 : 1;
+  static constexpr int EPI_WARPS = 4 * MT;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 };
 
-__device__ __forceinline__ bool tc_tile_of(const TcSched& sc, int task, int j, int& m_blk, int& n_blk, int& mm,
-                                           int& nn) {
-  const int mg = task % sc.num_mg, ng = task / sc.num_mg;
-  nn = j / sc.m_per_task;
-  mm = j % sc.m_per_task;
-  m_blk = mg * sc.m_per_task + mm;
-  n_blk = ng * sc.n_per_task + nn;
-  return m_blk < sc.num_m_blocks && n_blk < sc.num_n_blocks;
+struct TcSched {
+  int num_m_blocks;  // CTA row tiles (MT*128 rows loaded, m_step rows apart)
+  int num_n_blocks;  // 256-wide column blocks
+  int n_per_task;    // consecutive column blocks per task (the epilogue carries state across them)
+  int num_kb;        // 64-deep K blocks
+  int m_step;        // rows between consecutive row tiles: 64 (half tiles), 128 or 256
+  int group_m;       // raster: tasks cover group_m row tiles (row fastest), then the next columns
+  int num_ng;        // ceil(num_n_blocks / n_per_task)
+  int num_tasks;     // num_m_blocks * num_ng
+};
+
+__device__ __forceinline__ void tc_task_of(const TcSched& sc, int task, int& m_blk, int& ng) {
+  const int per_group = sc.group_m * sc.num_ng;
+  const int g = task / per_group, r = task % per_group;
+  const int gm = min(sc.group_m, sc.num_m_blocks - g * sc.group_m);
+  m_blk = g * sc.group_m + r % gm;
+  ng = r / gm;
 }
 
 // all lanes of the warp agree on the outcome of a bounded wait
@@ -69,16 +81,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-template <bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+template <int MT, bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(TcCfg<MT>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcSched sc, const int b_off_n, const int b_off_k, const typename Epi::Params ep,
                    int* status, const uint64_t timeout_ns) {
+  using C = TcCfg<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC_STAGES * TC_STAGE_BYTES);
-  uint64_t* empty = full + TC_STAGES;
-  uint64_t* tfull = empty + TC_STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -86,13 +99,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TC_STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], C::EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -118,10 +131,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       uint32_t pending = 0, pend_par = 0;  // per stage: load issued and its phase parity
       bool ok = true;
       for (int task = blockIdx.x; ok && task < sc.num_tasks; task += gridDim.x) {
-        const int ntile = sc.m_per_task * sc.n_per_task;
-        for (int j = 0; ok && j < ntile; ++j) {
-          int m_blk, n_blk, mm, nn;
-          if (!tc_tile_of(sc, task, j, m_blk, n_blk, mm, nn)) continue;
+        int m_blk, ng;
+        tc_task_of(sc, task, m_blk, ng);
+        for (int nn = 0; ok && nn < sc.n_per_task; ++nn) {
+          const int n_blk = ng * sc.n_per_task + nn;
+          if (n_blk >= sc.num_n_blocks) break;
           const int m0 = m_blk * sc.m_step;
           const int n0 = n_blk * TC_BN + b_off_n;
           for (int kb = 0; kb < sc.num_kb; ++kb) {
@@ -129,15 +143,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], TC_STAGE_BYTES);
-            uint8_t* sA = smem + stage * TC_STAGE_BYTES;
-            uint8_t* sB = sA + TC_A_BYTES;
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            uint8_t* sA = smem + stage * C::STAGE_BYTES;
+            uint8_t* sB = sA + MT * TC_A_BYTES;
             const int k0 = kb * TC_BK;
-            if (!A_MN) {
-              tma_load_2d(sA, &tmA, &full[stage], k0, m0);
-            } else {
-              tma_load_2d(sA, &tmA, &full[stage], m0, k0);
-              tma_load_2d(sA + 8192, &tmA, &full[stage], m0 + 64, k0);
+#pragma unroll
+            for (int q = 0; q < MT; ++q) {
+              if (!A_MN) {
+                tma_load_2d(sA + q * TC_A_BYTES, &tmA, &full[stage], k0, m0 + q * TC_BM);
+              } else {
+                tma_load_2d(sA + q * TC_A_BYTES, &tmA, &full[stage], m0 + q * TC_BM, k0);
+                tma_load_2d(sA + q * TC_A_BYTES + 8192, &tmA, &full[stage], m0 + q * TC_BM + 64, k0);
+              }
             }
             if (!B_MN) {
               tma_load_2d(sB, &tmB, &full[stage], k0 + b_off_k, n0);
@@ -147,7 +164,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             pending |= 1u << stage;
             pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == TC_STAGES) {
+            if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
@@ -156,7 +173,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       if (!ok) {
         // let every copy this thread issued land before shared memory is released
-        for (int s = 0; s < TC_STAGES; ++s)
+        for (int s = 0; s < C::STAGES; ++s)
           if (pending & (1u << s)) {
             volatile int no_abort = 0;
             mbar_wait_bounded(&full[s], (pend_par >> s) & 1u, &no_abort, nullptr, 0, timeout_ns);
@@ -173,10 +190,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
       for (int task = blockIdx.x; ok && task < sc.num_tasks; task += gridDim.x) {
-        const int ntile = sc.m_per_task * sc.n_per_task;
-        for (int j = 0; ok && j < ntile; ++j) {
-          int m_blk, n_blk, mm, nn;
-          if (!tc_tile_of(sc, task, j, m_blk, n_blk, mm, nn)) continue;
+        int m_blk, ng;
+        tc_task_of(sc, task, m_blk, ng);
+        for (int nn = 0; ok && nn < sc.n_per_task; ++nn) {
+          if (ng * sc.n_per_task + nn >= sc.num_n_blocks) break;
           if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, status, GH_DEV_TIMEOUT, timeout_ns)) {
             ok = false;
             break;
@@ -189,27 +206,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + stage * TC_STAGE_BYTES);
-            const uint32_t b_base = a_base + TC_A_BYTES;
+            const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
+            const uint32_t b_base = a_base + MT * TC_A_BYTES;
 #pragma unroll
             for (int kk = 0; kk < TC_BK / 16; ++kk) {
-              const uint64_t ad = A_MN ? sdesc_sw128(a_base + kk * 2048, 8192, 1024)
-                                       : sdesc_sw128(a_base + kk * 32, 16, 1024);
               const uint64_t bd = B_MN ? sdesc_sw128(b_base + kk * 2048, 8192, 1024)
                                        : sdesc_sw128(b_base + kk * 32, 16, 1024);
-              umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+              for (int q = 0; q < MT; ++q) {
+                const uint32_t aq = a_base + q * TC_A_BYTES;
+                const uint64_t ad = A_MN ? sdesc_sw128(aq + kk * 2048, 8192, 1024)
+                                         : sdesc_sw128(aq + kk * 32, 16, 1024);
+                umma_bf16(d_tmem + static_cast<uint32_t>(q * TC_BN), ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+              }
             }
             issued = true;
             umma_commit(&empty[stage]);
-            if (++stage == TC_STAGES) {
+            if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
           umma_commit(&tfull[acc]);
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1u;
+          if (C::NUM_ACC == 2) {
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+          } else {
+            acc_phase ^= 1u;
+          }
         }
       }
       if (issued) {
@@ -221,33 +246,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   } else {
-    // -------------------------------------------------- epilogue warps 2..5
-    const int sub = warp & 3;  // TMEM lane quarter this warp may access
-    const int row = sub * 32 + lane;
-    const uint32_t lane_addr = static_cast<uint32_t>(sub * 32) << 16;
+    // -------------------------------------------------- epilogue warps
+    const int ew = warp - 2;
+    const int q = ew >> 2;      // which 128-row block of the tile
+    const int sub = warp & 3;   // TMEM lane quarter this warp may access
+    const int row = q * TC_BM + sub * 32 + lane;  // row within the CTA tile
+    const uint32_t lane_addr = (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(q * TC_BN);
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     Epi epi;
     for (int task = blockIdx.x; ok && task < sc.num_tasks; task += gridDim.x) {
-      epi.begin_task(ep, sc, task, row);
-      const int ntile = sc.m_per_task * sc.n_per_task;
-      for (int j = 0; ok && j < ntile; ++j) {
-        int m_blk, n_blk, mm, nn;
-        if (!tc_tile_of(sc, task, j, m_blk, n_blk, mm, nn)) continue;
+      int m_blk, ng;
+      tc_task_of(sc, task, m_blk, ng);
+      epi.begin_task(ep, sc, m_blk, row);
+      for (int nn = 0; ok && nn < sc.n_per_task; ++nn) {
+        const int n_blk = ng * sc.n_per_task + nn;
+        if (n_blk >= sc.num_n_blocks) break;
         if (!warp_wait(&tfull[acc], acc_phase, abort_flag, status, timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        epi.tile(ep, sc, tmem_base + lane_addr + static_cast<uint32_t>(acc * TC_BN), m_blk, n_blk, mm, row);
+        epi.tile(ep, sc, tmem_base + lane_addr + static_cast<uint32_t>(acc * TC_BN), m_blk, n_blk, row);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (C::NUM_ACC == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;
+        }
       }
-      if (ok) epi.end_task(ep, sc, task, row);
+      if (ok) epi.end_task(ep, sc, m_blk, ng, row);
     }
   }
 
@@ -273,26 +305,21 @@ struct EpiFwdLse {
     float* zy;      // [N]
     const int* targets;
   };
-  float m[2], s[2];
-  int y[2];
+  float m, s;
+  int y, grow;
+  bool valid;
 
-  __device__ __forceinline__ void begin_task(const Params& p, const TcSched& sc, int task, int row) {
-    const int mg = task % sc.num_mg;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      m[q] = -INFINITY;
-      s[q] = 0.f;
-      const int grow = (mg * sc.m_per_task + q) * sc.m_step + row;
-      y[q] = (q < sc.m_per_task && row < sc.m_step && grow < p.N) ? __ldg(p.targets + grow) : -1;
-    }
+  __device__ __forceinline__ void begin_task(const Params& p, const TcSched& sc, int m_blk, int row) {
+    m = -INFINITY;
+    s = 0.f;
+    grow = m_blk * sc.m_step + row;
+    valid = row < sc.m_step && grow < p.N;
+    y = valid ? __ldg(p.targets + grow) : -1;
   }
 
-  __device__ __forceinline__ void tile(const Params& p, const TcSched& sc, uint32_t taddr, int m_blk, int n_blk,
-                                       int mm, int row) {
-    float run_m = mm ? m[1] : m[0];
-    float run_s = mm ? s[1] : s[0];
-    const int yy = mm ? y[1] : y[0];
-    const int grow = m_blk * sc.m_step + row;
+  __device__ __forceinline__ void tile(const Params& p, const TcSched&, uint32_t taddr, int, int n_blk, int) {
+    float run_m = m, run_s = s;
+    const int yy = y;
 #pragma unroll 1
     for (int c = 0; c < TC_BN / 32; ++c) {
       float v[32];
@@ -331,27 +358,14 @@ struct EpiFwdLse {
         run_m = mnew;
       }
     }
-    if (mm) {
-      m[1] = run_m;
-      s[1] = run_s;
-    } else {
-      m[0] = run_m;
-      s[0] = run_s;
-    }
+    m = run_m;
+    s = run_s;
   }
 
-  __device__ __forceinline__ void end_task(const Params& p, const TcSched& sc, int task, int row) {
-    const int mg = task % sc.num_mg, split = task / sc.num_mg;
-    if (row >= sc.m_step) return;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int m_blk = mg * sc.m_per_task + q;
-      const int grow = m_blk * sc.m_step + row;
-      if (q < sc.m_per_task && m_blk < sc.num_m_blocks && grow < p.N) {
-        p.part_m[static_cast<size_t>(split) * p.N + grow] = m[q];
-        p.part_s[static_cast<size_t>(split) * p.N + grow] = s[q];
-      }
-    }
+  __device__ __forceinline__ void end_task(const Params& p, const TcSched&, int, int split, int) {
+    if (!valid) return;
+    p.part_m[static_cast<size_t>(split) * p.N + grow] = m;
+    p.part_s[static_cast<size_t>(split) * p.N + grow] = s;
   }
 };
 
@@ -372,10 +386,10 @@ struct EpiDlogits {
     __nv_bfloat16* G;
   };
   __device__ __forceinline__ void begin_task(const Params&, const TcSched&, int, int) {}
-  __device__ __forceinline__ void end_task(const Params&, const TcSched&, int, int) {}
+  __device__ __forceinline__ void end_task(const Params&, const TcSched&, int, int, int) {}
 
   __device__ __forceinline__ void tile(const Params& p, const TcSched& sc, uint32_t taddr, int m_blk, int n_blk,
-                                       int, int row) {
+                                       int row) {
     const int grow = m_blk * sc.m_step + row;
     const bool valid = grow < p.N;
     const float g = p.grad_out ? __ldg(p.grad_out) : 1.f;
@@ -424,10 +438,10 @@ struct EpiStore {
     __nv_bfloat16* out16;
   };
   __device__ __forceinline__ void begin_task(const Params&, const TcSched&, int, int) {}
-  __device__ __forceinline__ void end_task(const Params&, const TcSched&, int, int) {}
+  __device__ __forceinline__ void end_task(const Params&, const TcSched&, int, int, int) {}
 
   __device__ __forceinline__ void tile(const Params& p, const TcSched& sc, uint32_t taddr, int m_blk, int n_blk,
-                                       int, int row) {
+                                       int row) {
     const int lrow = m_blk * sc.m_step + row;
     const bool valid = lrow < p.M_valid;
     const size_t rbase = static_cast<size_t>(p.row_off + lrow) * p.ld;

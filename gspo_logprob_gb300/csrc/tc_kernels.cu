@@ -1,5 +1,7 @@
 // tcgen05 kernels of the bf16 path: logits + online LSE (forward), dlogits
 // recompute (backward) and the dH / dW GEMMs, all instances of tc_gemm_kernel.
+#include <cstdlib>
+
 #include "internal.h"
 #include "tc_gemm.cuh"
 
@@ -7,32 +9,77 @@ namespace gh {
 
 namespace {
 
-template <bool A_MN, bool B_MN, class Epi>
+// Tuning knobs (read once from the environment): CTA row-tile height of each
+// backward GEMM (1 or 2 blocks of 128 rows) and the raster group size.  Every
+// setting computes the same result; they only change tile shape and order.
+int env_int(const char* name, int dflt) {
+  const char* e = getenv(name);
+  return e ? atoi(e) : dflt;
+}
+// per kernel kind: 1 = 128 x 256 tiles (double-buffered accumulator), 2 = 256 x 256.
+// Defaults from a sweep on the 8B-vocabulary workload: dlogits and dW run 256-row
+// tiles (their epilogues are short next to K); dH keeps 128-row tiles because
+// its fp32 read-modify-write epilogue needs the second accumulator to hide.
+int kind_mt(const char* name, int dflt) {
+  const int v = env_int(name, dflt);
+  return v == 1 || v == 2 ? v : dflt;
+}
+int dlogits_mt() {
+  static const int v = kind_mt("GH_DLOGITS_MT", 2);
+  return v;
+}
+int dh_mt() {
+  static const int v = kind_mt("GH_DH_MT", 1);
+  return v;
+}
+int dw_mt() {
+  static const int v = kind_mt("GH_DW_MT", 2);
+  return v;
+}
+int kind_group_m(const char* name, int dflt) {
+  const int v = env_int(name, dflt);
+  return v > 0 ? v : dflt;
+}
+int dlogits_group_m() {
+  static const int v = kind_group_m("GH_DLOGITS_GROUP_M", 16);
+  return v;
+}
+int dh_group_m() {
+  static const int v = kind_group_m("GH_DH_GROUP_M", 4);
+  return v;
+}
+int dw_group_m() {
+  static const int v = kind_group_m("GH_DW_GROUP_M", 4);
+  return v;
+}
+
+template <int MT, bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const TcSched& sc, int b_off_n, int b_off_k,
                       const typename Epi::Params& ep, int* status, cudaStream_t st) {
-  auto kern = tc_gemm_kernel<A_MN, B_MN, Epi>;
+  using C = TcCfg<MT>;
+  auto kern = tc_gemm_kernel<MT, A_MN, B_MN, Epi>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (sc.num_tasks <= 0) return cudaSuccess;
   const int grid = static_cast<int>(sc.num_tasks < num_sms() ? sc.num_tasks : num_sms());
-  kern<<<grid, TC_THREADS, TC_SMEM_BYTES, st>>>(ta, tb, sc, b_off_n, b_off_k, ep, status, timeout_ns());
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, sc, b_off_n, b_off_k, ep, status, timeout_ns());
   return cudaGetLastError();
 }
 
-TcSched make_sched(int num_m_blocks, int num_n_blocks, int m_per_task, int n_per_task, int num_kb, int m_step) {
+TcSched make_sched(int num_m_blocks, int num_n_blocks, int n_per_task, int num_kb, int m_step, int group_m) {
   TcSched sc;
   sc.num_m_blocks = num_m_blocks;
   sc.num_n_blocks = num_n_blocks;
-  sc.m_per_task = m_per_task;
   sc.n_per_task = n_per_task;
   sc.num_kb = num_kb;
   sc.m_step = m_step;
-  sc.num_mg = static_cast<int>(ceil_div(num_m_blocks, m_per_task));
-  sc.num_tasks = sc.num_mg * static_cast<int>(ceil_div(num_n_blocks, n_per_task));
+  sc.group_m = group_m < 1 ? 1 : (group_m > num_m_blocks ? num_m_blocks : group_m);
+  sc.num_ng = static_cast<int>(ceil_div(num_n_blocks, n_per_task));
+  sc.num_tasks = num_m_blocks * sc.num_ng;
   return sc;
 }
 
@@ -43,11 +90,8 @@ cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st) {
   // A = H [N, D] K-major, B = W [V, D] K-major
   if (!make_tmap_bf16(&ta, a.H, a.D, a.N, static_cast<uint64_t>(a.D) * 2, TC_BK, TC_BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, a.W, a.D, a.V, static_cast<uint64_t>(a.D) * 2, TC_BK, TC_BN)) return cudaErrorInvalidValue;
-  const int m_step = a.row_tile == 64 ? 64 : 128;
-  const int m_per_task = a.row_tile == 256 ? 2 : 1;
-  const int num_m = static_cast<int>(ceil_div(a.N, m_step));
   const int num_vt = static_cast<int>(ceil_div(a.V, VTILE));
-  TcSched sc = make_sched(num_m, num_vt, m_per_task, TILES_PER_SPLIT, static_cast<int>(ceil_div(a.D, TC_BK)), m_step);
+  const int nkb = static_cast<int>(ceil_div(a.D, TC_BK));
   EpiFwdLse::Params ep;
   ep.N = a.N;
   ep.V = a.V;
@@ -55,15 +99,23 @@ cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st) {
   ep.part_s = a.part_s;
   ep.zy = a.zy;
   ep.targets = a.targets;
-  return launch_tc<false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);
+  // every row tile of a split before the next split: the split's W tiles are
+  // shared in L2 by all CTAs working on it
+  if (a.row_tile == 64 || a.row_tile == 128) {
+    const int m_step = a.row_tile;
+    const int num_m = static_cast<int>(ceil_div(a.N, m_step));
+    TcSched sc = make_sched(num_m, num_vt, TILES_PER_SPLIT, nkb, m_step, num_m);
+    return launch_tc<1, false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);
+  }
+  const int num_m = static_cast<int>(ceil_div(a.N, 2 * TC_BM));
+  TcSched sc = make_sched(num_m, num_vt, TILES_PER_SPLIT, nkb, 2 * TC_BM, num_m);
+  return launch_tc<2, false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);
 }
 
 cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, a.H, a.D, a.N, static_cast<uint64_t>(a.D) * 2, TC_BK, TC_BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, a.W, a.D, a.V, static_cast<uint64_t>(a.D) * 2, TC_BK, TC_BN)) return cudaErrorInvalidValue;
-  TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, TC_BM)), static_cast<int>(ceil_div(a.width, TC_BN)), 1, 1,
-                          static_cast<int>(ceil_div(a.D, TC_BK)), TC_BM);
   EpiDlogits::Params ep;
   ep.N = a.N;
   ep.V = a.V;
@@ -74,7 +126,14 @@ cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st) {
   ep.grad_out = a.grad_out;
   ep.targets = a.targets;
   ep.G = static_cast<__nv_bfloat16*>(a.G);
-  return launch_tc<false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
+  const int nkb = static_cast<int>(ceil_div(a.D, TC_BK));
+  const int nn = static_cast<int>(ceil_div(a.width, TC_BN));
+  if (dlogits_mt() == 1) {
+    TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, TC_BM)), nn, 1, nkb, TC_BM, dlogits_group_m());
+    return launch_tc<1, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
+  }
+  TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dlogits_group_m());
+  return launch_tc<2, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
 }
 
 cudaError_t launch_dh_tc(const TcDhArgs& a, cudaStream_t st) {
@@ -82,8 +141,6 @@ cudaError_t launch_dh_tc(const TcDhArgs& a, cudaStream_t st) {
   // A = G [N, ldg] K-major (K = vocabulary column); B = W [V, D] MN-major (N = D, K = vocabulary row)
   if (!make_tmap_bf16(&ta, a.G, a.ldg, a.N, static_cast<uint64_t>(a.ldg) * 2, TC_BK, TC_BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, a.W, a.D, a.V, static_cast<uint64_t>(a.D) * 2, 64, TC_BK)) return cudaErrorInvalidValue;
-  TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, TC_BM)), static_cast<int>(ceil_div(a.D, TC_BN)), 1, 1,
-                          static_cast<int>(ceil_div(a.width, TC_BK)), TC_BM);
   EpiStore::Params ep;
   ep.M_valid = a.N;
   ep.N_valid = a.D;
@@ -92,7 +149,14 @@ cudaError_t launch_dh_tc(const TcDhArgs& a, cudaStream_t st) {
   ep.mode = a.mode;
   ep.out32 = a.acc32;
   ep.out16 = static_cast<__nv_bfloat16*>(a.out16);
-  return launch_tc<false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
+  const int nkb = static_cast<int>(ceil_div(a.width, TC_BK));
+  const int nn = static_cast<int>(ceil_div(a.D, TC_BN));
+  if (dh_mt() == 1) {
+    TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, TC_BM)), nn, 1, nkb, TC_BM, dh_group_m());
+    return launch_tc<1, false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
+  }
+  TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dh_group_m());
+  return launch_tc<2, false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
 }
 
 cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st) {
@@ -102,8 +166,6 @@ cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st) {
   if (!make_tmap_bf16(&ta, a.G, a.ldg, a.N, static_cast<uint64_t>(a.ldg) * 2, 64, TC_BK)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, a.H, a.D, a.N, static_cast<uint64_t>(a.D) * 2, 64, TC_BK)) return cudaErrorInvalidValue;
   const int rows = a.V - a.vb0 < a.width ? a.V - a.vb0 : a.width;
-  TcSched sc = make_sched(static_cast<int>(ceil_div(rows, TC_BM)), static_cast<int>(ceil_div(a.D, TC_BN)), 1, 1,
-                          static_cast<int>(ceil_div(a.N, TC_BK)), TC_BM);
   EpiStore::Params ep;
   ep.M_valid = rows;
   ep.N_valid = a.D;
@@ -112,7 +174,14 @@ cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st) {
   ep.mode = a.accumulate ? 1 : 0;
   ep.out32 = a.dW;
   ep.out16 = nullptr;
-  return launch_tc<true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
+  const int nkb = static_cast<int>(ceil_div(a.N, TC_BK));
+  const int nn = static_cast<int>(ceil_div(a.D, TC_BN));
+  if (dw_mt() == 1) {
+    TcSched sc = make_sched(static_cast<int>(ceil_div(rows, TC_BM)), nn, 1, nkb, TC_BM, dw_group_m());
+    return launch_tc<1, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
+  }
+  TcSched sc = make_sched(static_cast<int>(ceil_div(rows, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dw_group_m());
+  return launch_tc<2, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
 }
 
 }  // namespace gh

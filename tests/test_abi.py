@@ -78,9 +78,12 @@ def test_workspace_sizes(lib):
     fw = lib.grpo_head_forward_workspace_size(ctypes.byref(h))
     al = lambda x: (x + 255) // 256 * 256
     assert fw == 2 * al(5 * 1000 * 4) + al(1000 * 4)
-    # backward (bf16): G block of min(5120, 4096) columns, plus the fp32 dH accumulator (2 blocks)
+    # backward (bf16): one block of all 5120 padded columns, no dH accumulator
     bw = lib.grpo_head_backward_workspace_size(ctypes.byref(h))
-    assert bw == al(1000 * 4096 * 2) + al(1000 * 256 * 4)
+    assert bw == al(1000 * 5120 * 2)
+    # a vocabulary of two 16384-column blocks adds the fp32 dH accumulator
+    h3 = _head(N=1000, D=256, V=20000)
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h3)) == al(1000 * 16384 * 2) + al(1000 * 256 * 4)
     # a single-block vocabulary needs no accumulator
     h2 = _head(N=64, D=64, V=500)
     assert lib.grpo_head_backward_workspace_size(ctypes.byref(h2)) == al(64 * 512 * 2)
