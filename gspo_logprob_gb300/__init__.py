@@ -12,7 +12,8 @@ machine without the built library; the first call then fails loudly if the
 library is missing.
 """
 __all__ = ["grpo_head_forward", "gspo_segment_loss", "grpo_head_backward", "grpo_group_advantage",
-           "build", "ops"]
+           "grpo_loss_from_sequence_totals", "grpo_head_logprob_shard", "grpo_logprob_merge",
+           "vocab_shard_bounds", "build", "ops"]
 
 
 def build(verbose: bool = False) -> str:
@@ -21,7 +22,9 @@ def build(verbose: bool = False) -> str:
 
 
 def __getattr__(name):
-    if name in ("grpo_head_forward", "gspo_segment_loss", "grpo_head_backward", "grpo_group_advantage", "ops"):
+    if name in ("grpo_head_forward", "gspo_segment_loss", "grpo_head_backward", "grpo_group_advantage",
+                "grpo_loss_from_sequence_totals", "grpo_head_logprob_shard", "grpo_logprob_merge",
+                "vocab_shard_bounds", "ops"):
         import importlib
         ops = importlib.import_module(".ops", __name__)
         return ops if name == "ops" else getattr(ops, name)

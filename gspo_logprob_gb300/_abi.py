@@ -21,7 +21,8 @@ DEV_BIT_NAMES = {1: "TARGET_OOR", 2: "NONFINITE", 4: "TIMEOUT", 8: "NO_ACTIVE", 
 GH_BF16, GH_FP32 = 0, 1
 GH_TOKEN_MEAN, GH_SEQ_MEAN, GH_FIXED = 0, 1, 2
 REDUCTIONS = {"token_mean": GH_TOKEN_MEAN, "seq_mean": GH_SEQ_MEAN, "fixed": GH_FIXED}
-NUM_KERNEL_KINDS = 12
+RATIO_LEVELS = {"token": 0, "sequence": 1}
+NUM_KERNEL_KINDS = 14
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # GH_NOALLOC_SCRATCH_BYTES
 
 
@@ -33,7 +34,8 @@ class GhHead(ctypes.Structure):
 class GhGrpo(ctypes.Structure):
     _fields_ = [("old_logp", c_void_p), ("ref_logp", c_void_p), ("adv", c_void_p), ("seq_id", c_void_p),
                 ("num_seqs", c_int32), ("reduction", c_int32), ("eps_low", c_float), ("eps_high", c_float),
-                ("beta", c_float), ("reserved", c_float), ("norm", c_double)]
+                ("beta", c_float), ("delta", c_float), ("norm", c_double), ("ratio_level", c_int32),
+                ("reserved", c_int32), ("seq_policy", c_void_p), ("seq_kl", c_void_p), ("seq_count", c_void_p)]
 
 
 # name -> (restype, argtypes)
@@ -50,6 +52,13 @@ SIGNATURES = {
     "grpo_group_advantage": (c_int32, [c_void_p, c_int32, c_int32, c_float, c_void_p, c_void_p, c_void_p]),
     "grpo_head_forward_noalloc": (c_int32, [POINTER(GhHead), POINTER(GhGrpo), c_void_p, c_void_p, c_void_p,
                                             c_void_p, c_void_p, c_void_p]),
+    "gh_vocab_shard_bounds": (c_int32, [c_int64, c_int32, c_int32, POINTER(c_int64), POINTER(c_int64)]),
+    "grpo_head_logprob_shard": (c_int32, [POINTER(GhHead), c_int64, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          c_void_p]),
+    "grpo_logprob_merge": (c_int32, [c_int64, c_int64, c_int32, POINTER(c_int64), c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "grpo_loss_from_sequence_totals": (c_int32, [c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_double, c_float,
+                                                 c_void_p, c_void_p, c_void_p]),
     "gh_status_string": (c_char_p, [c_int32]),
     "gh_last_error": (c_char_p, []),
     "gh_abi_version": (c_int32, []),

@@ -237,7 +237,7 @@ using namespace gh;
 
 extern "C" {
 
-int32_t gh_abi_version(void) { return 100; }
+int32_t gh_abi_version(void) { return 101; }
 
 const char* gh_status_string(gh_status s) {
   switch (s) {
@@ -282,6 +282,11 @@ gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* log
       return fail(GH_ERR_INVALID_ARG, "fixed reduction needs norm > 0");
     if (!(grpo->eps_low >= 0.f) || !(grpo->eps_high >= 0.f) || !std::isfinite(grpo->beta) || grpo->norm < 0.0)
       return fail(GH_ERR_INVALID_ARG, "eps_low/eps_high/beta/norm invalid");
+    if (!(grpo->delta >= 0.f) || !std::isfinite(grpo->delta))
+      return fail(GH_ERR_INVALID_ARG, "delta must be finite and >= 0 (0 = no cap)");
+    if (grpo->ratio_level != 0 && grpo->ratio_level != 1)
+      return fail(GH_ERR_INVALID_ARG, "ratio_level=%d (expected 0 token or 1 sequence)", grpo->ratio_level);
+    if (grpo->reserved != 0) return fail(GH_ERR_INVALID_ARG, "gh_grpo.reserved must be 0");
   }
   const size_t need = fwd_layout(head, nullptr).bytes;
   if (need > 0 && (!ws || ws_bytes < need))
@@ -311,6 +316,109 @@ gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* log
     cudaError_t e = run(K_GRPO, st, [&] { return launch_grpo(N, logp, head->mask, grpo, coef, loss3, status, st); });
     if (e != cudaSuccess) return cuda_fail(e, "GRPO loss launch");
   }
+  return GH_OK;
+}
+
+gh_status gh_vocab_shard_bounds(int64_t V_total, int32_t num_shards, int32_t rank, int64_t* start, int64_t* len) {
+  g_last_error.clear();
+  if (!start || !len) return fail(GH_ERR_INVALID_ARG, "start/len is NULL");
+  if (V_total < 1) return fail(GH_ERR_INVALID_ARG, "V_total must be >= 1");
+  const int64_t S = ceil_div(V_total, SPLIT_COLS);
+  if (num_shards < 1 || num_shards > MAX_SHARDS || num_shards > S)
+    return fail(GH_ERR_INVALID_ARG, "num_shards=%d must be in [1, min(%d, %lld splits)]", num_shards, MAX_SHARDS,
+                (long long)S);
+  if (rank < 0 || rank >= num_shards) return fail(GH_ERR_INVALID_ARG, "rank out of range");
+  const int64_t base = S / num_shards, extra = S % num_shards;
+  const int64_t s0 = rank * base + (rank < extra ? rank : extra);
+  const int64_t ns = base + (rank < extra ? 1 : 0);
+  const int64_t c0 = s0 * SPLIT_COLS;
+  const int64_t c1 = (s0 + ns) * SPLIT_COLS < V_total ? (s0 + ns) * SPLIT_COLS : V_total;
+  *start = c0;
+  *len = c1 - c0;
+  return GH_OK;
+}
+
+gh_status grpo_head_logprob_shard(const gh_head* head, int64_t vocab_start, int64_t V_total, float* part_m,
+                                  float* part_s, float* zy, int32_t* status, void* stream) {
+  g_last_error.clear();
+  gh_status s = check_head(head);
+  if (s != GH_OK) return s;
+  if (!status) return fail(GH_ERR_INVALID_ARG, "status is NULL");
+  if (head->N > 0 && (!part_m || !part_s || !zy)) return fail(GH_ERR_INVALID_ARG, "part_m/part_s/zy is NULL");
+  if (vocab_start < 0 || vocab_start % SPLIT_COLS != 0)
+    return fail(GH_ERR_INVALID_ARG, "vocab_start=%lld must be a multiple of %d", (long long)vocab_start, SPLIT_COLS);
+  if (V_total > (int64_t(1) << 28) || vocab_start + head->V > V_total)
+    return fail(GH_ERR_INVALID_ARG, "shard [%lld, %lld) exceeds V_total=%lld", (long long)vocab_start,
+                (long long)(vocab_start + head->V), (long long)V_total);
+  if (vocab_start + head->V < V_total && head->V % SPLIT_COLS != 0)
+    return fail(GH_ERR_INVALID_ARG, "a shard other than the last must hold whole %d-column splits", SPLIT_COLS);
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int N = static_cast<int>(head->N), D = static_cast<int>(head->D), V = static_cast<int>(head->V);
+  if (N == 0) return GH_OK;
+  cudaError_t e;
+  if (head->dtype == GH_BF16) {
+    TcFwdArgs a{N, D, V, head->row_tile, head->H, head->W, head->targets, part_m, part_s, zy, status,
+                static_cast<int>(vocab_start)};
+    e = run(K_FWD_TC, st, [&] { return launch_fwd_tc(a, st); });
+  } else {
+    F32FwdArgs a{N, D, V, head->row_tile, static_cast<const float*>(head->H), static_cast<const float*>(head->W),
+                 head->targets, part_m, part_s, zy, static_cast<int>(vocab_start)};
+    e = run(K_FWD_F32, st, [&] { return launch_fwd_f32(a, st); });
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "shard forward launch");
+  return GH_OK;
+}
+
+gh_status grpo_logprob_merge(int64_t N, int64_t V_total, int32_t num_shards, const int64_t* shard_starts,
+                             const float* part_m, const float* part_s, const float* zy, const int32_t* targets,
+                             const uint8_t* mask, float* logp, float* lse, int32_t* status, void* stream) {
+  g_last_error.clear();
+  if (N < 0 || N > (int64_t(1) << 30)) return fail(GH_ERR_INVALID_ARG, "N out of range");
+  if (V_total < 1 || V_total > (int64_t(1) << 28)) return fail(GH_ERR_INVALID_ARG, "V_total out of range");
+  if (!status || !shard_starts) return fail(GH_ERR_INVALID_ARG, "status/shard_starts is NULL");
+  if (N > 0 && (!part_m || !part_s || !zy || !targets || !mask || !logp || !lse))
+    return fail(GH_ERR_INVALID_ARG, "a tensor pointer is NULL");
+  if (num_shards < 1 || num_shards > MAX_SHARDS)
+    return fail(GH_ERR_INVALID_ARG, "num_shards=%d out of [1, %d]", num_shards, MAX_SHARDS);
+  ShardBounds sb;
+  sb.num_shards = num_shards;
+  if (shard_starts[0] != 0 || shard_starts[num_shards] != V_total)
+    return fail(GH_ERR_INVALID_ARG, "shard bounds must start at 0 and end at V_total");
+  for (int r = 0; r < num_shards; ++r) {
+    if (shard_starts[r + 1] <= shard_starts[r] || shard_starts[r] % SPLIT_COLS != 0)
+      return fail(GH_ERR_INVALID_ARG, "shard %d bounds [%lld, %lld) are not increasing multiples of %d", r,
+                  (long long)shard_starts[r], (long long)shard_starts[r + 1], SPLIT_COLS);
+    sb.start[r] = static_cast<int>(shard_starts[r]);
+  }
+  sb.start[num_shards] = static_cast<int>(V_total);
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = run(K_MERGE_SHARDS, st, [&] {
+    return launch_merge_shards(static_cast<int>(N), static_cast<int>(V_total), static_cast<int>(num_splits(V_total)),
+                               part_m, part_s, zy, sb, targets, mask, logp, lse, status, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "shard merge launch");
+  return GH_OK;
+}
+
+gh_status grpo_loss_from_sequence_totals(int32_t num_seqs, const float* seq_policy, const float* seq_kl,
+                                         const int32_t* seq_count, int32_t reduction, double norm, float beta,
+                                         float* loss3, int32_t* status, void* stream) {
+  g_last_error.clear();
+  if (!seq_policy || !seq_kl || !seq_count || !loss3 || !status)
+    return fail(GH_ERR_INVALID_ARG, "seq_policy/seq_kl/seq_count/loss3/status is NULL");
+  if (num_seqs < 1 || num_seqs > MAX_SEQS)
+    return fail(GH_ERR_INVALID_ARG, "num_seqs=%d out of [1, %d]", num_seqs, MAX_SEQS);
+  if (reduction < GH_TOKEN_MEAN || reduction > GH_FIXED) return fail(GH_ERR_INVALID_ARG, "reduction=%d unknown", reduction);
+  if (reduction == GH_FIXED && !(norm > 0.0)) return fail(GH_ERR_INVALID_ARG, "fixed reduction needs norm > 0");
+  if (norm < 0.0 || !std::isfinite(beta)) return fail(GH_ERR_INVALID_ARG, "norm/beta invalid");
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = run(K_GRPO_TOTALS, st, [&] {
+    return launch_grpo_totals(num_seqs, seq_policy, seq_kl, seq_count, reduction, norm, beta, loss3, status, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "sequence-totals launch");
   return GH_OK;
 }
 
@@ -451,7 +559,8 @@ int64_t gh_launch_count(void) { return g_prof.launches_total; }
 const char* gh_kernel_kind_name(int32_t kind) {
   static const char* names[GH_NUM_KERNEL_KINDS] = {
       "fwd_logits_lse_tc", "merge_lse", "grpo_loss", "gspo_segment", "dlogits_tc", "dh_gemm_tc",
-      "dw_gemm_tc", "group_advantage", "fwd_logits_lse_f32", "dlogits_f32", "gemm_f32", "timeout_probe"};
+      "dw_gemm_tc", "group_advantage", "fwd_logits_lse_f32", "dlogits_f32", "gemm_f32", "timeout_probe",
+      "grpo_sequence_totals", "merge_lse_shards"};
   if (kind < 0 || kind >= GH_NUM_KERNEL_KINDS) return "";
   return names[kind];
 }

@@ -37,6 +37,8 @@ enum KernelKind {
   K_DLOGITS_F32 = 9,
   K_GEMM_F32 = 10,
   K_PROBE = 11,
+  K_GRPO_TOTALS = 12,
+  K_MERGE_SHARDS = 13,
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -66,6 +68,7 @@ struct TcFwdArgs {
   float* part_s;
   float* zy;
   int* status;
+  int col_offset;  // vocabulary shards: global id of local column 0 (else 0)
 };
 cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st);
 
@@ -79,6 +82,7 @@ struct TcDlogitsArgs {
   const float* grad_out;
   void* G;
   int* status;
+  int col_offset;
 };
 cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st);
 
@@ -112,6 +116,7 @@ struct F32FwdArgs {
   float* part_m;
   float* part_s;
   float* zy;
+  int col_offset;
 };
 cudaError_t launch_fwd_f32(const F32FwdArgs& a, cudaStream_t st);
 
@@ -124,6 +129,7 @@ struct F32DlogitsArgs {
   const float* coef;
   const float* grad_out;
   float* G;
+  int col_offset;
 };
 cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st);
 
@@ -145,8 +151,20 @@ cudaError_t launch_gemm_f32(const F32GemmArgs& a, cudaStream_t st);
 cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const float* part_s, const float* zy,
                          const int32_t* targets, const uint8_t* mask, float* logp, float* lse, int* status,
                          cudaStream_t st);
+// Shard bounds (global vocabulary ids, num_shards + 1 entries) for the merge of
+// vocabulary-parallel partials; zy is [num_shards, N].
+constexpr int MAX_SHARDS = 64;
+struct ShardBounds {
+  int num_shards;
+  int start[MAX_SHARDS + 1];
+};
+cudaError_t launch_merge_shards(int N, int V_total, int splits, const float* part_m, const float* part_s,
+                                const float* zy, const ShardBounds& sb, const int32_t* targets, const uint8_t* mask,
+                                float* logp, float* lse, int* status, cudaStream_t st);
 cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_grpo* g, float* coef,
                         float* loss3, int* status, cudaStream_t st);
+cudaError_t launch_grpo_totals(int num_seqs, const float* seq_policy, const float* seq_kl, const int32_t* seq_count,
+                               int reduction, double norm, float beta, float* loss3, int* status, cudaStream_t st);
 cudaError_t launch_gspo(int N, const float* logp, const float* old_logp, const uint8_t* mask,
                         const int32_t* seg_id, int num_segments, const float* seg_adv, float eps_low,
                         float eps_high, double divisor, int token_weighted, float* loss, float* seg_ratio,

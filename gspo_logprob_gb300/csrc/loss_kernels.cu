@@ -69,6 +69,43 @@ __global__ void merge_kernel(int N, int V, int splits, const float* __restrict__
   if (!isfinite(L) || (act && y >= 0 && y < V && !isfinite(lp))) atomicOr(status, GH_DEV_NONFINITE);
 }
 
+// merge of vocabulary-parallel partials: the splits of all shards in global
+// order (the same fold as merge_kernel), the target logit from the shard that
+// owns the target column
+__global__ void merge_shards_kernel(int N, int V_total, int splits, const float* __restrict__ part_m,
+                                    const float* __restrict__ part_s, const float* __restrict__ zy,
+                                    const ShardBounds sb, const int* __restrict__ targets,
+                                    const uint8_t* __restrict__ mask, float* logp, float* lse, int* status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  float M = -INFINITY;
+  for (int k = 0; k < splits; ++k) M = fmaxf(M, part_m[static_cast<size_t>(k) * N + i]);
+  float S = 0.f;
+  if (M != -INFINITY) {
+    for (int k = 0; k < splits; ++k) {
+      const float mk = part_m[static_cast<size_t>(k) * N + i];
+      if (mk != -INFINITY) S += part_s[static_cast<size_t>(k) * N + i] * expf(mk - M);
+    }
+  }
+  const float L = M + logf(S);
+  lse[i] = L;
+  const int y = targets[i];
+  const bool act = mask[i] != 0;
+  float lp;
+  if (y >= 0 && y < V_total) {
+    int owner = 0;
+    while (owner + 1 < sb.num_shards && y >= sb.start[owner + 1]) ++owner;
+    lp = zy[static_cast<size_t>(owner) * N + i] - L;
+  } else if (act) {
+    lp = __int_as_float(0x7fc00000);
+    atomicOr(status, GH_DEV_TARGET_OOR);
+  } else {
+    lp = 0.f;
+  }
+  logp[i] = lp;
+  if (!isfinite(L) || (act && y >= 0 && y < V_total && !isfinite(lp))) atomicOr(status, GH_DEV_NONFINITE);
+}
+
 // ---------------------------------------------------------------- GRPO
 struct GrpoP {
   int N;
@@ -80,10 +117,14 @@ struct GrpoP {
   const uint8_t* mask;
   int num_seqs;
   int reduction;
-  float eps_low, eps_high, beta;
+  float eps_low, eps_high, beta, delta;
+  int seq_level;
   double norm;
   float* coef;
   float* loss3;
+  float* seq_policy;
+  float* seq_kl;
+  int* seq_count;
   int* status;
 };
 
@@ -92,15 +133,99 @@ struct TokTerms {
   bool act;
 };
 
-__device__ __forceinline__ TokTerms grpo_terms(float lp, float od, float rf, float A, float lo, float hi) {
+// Token objective for ratio r: u = min(r, delta) A (cap off when delta <= 0),
+// v = clip(r, lo, hi) A, pg = -min(u, v); d pg / d log r = -A r act where act
+// follows the active branch (ties count as the unclipped term): the unclipped
+// term moves with r unless the cap binds, the clipped one only inside the band.
+__device__ __forceinline__ TokTerms grpo_terms(float r, float lp, float rf, float A, float lo, float hi,
+                                               float delta) {
   TokTerms t;
-  t.r = expf(lp - od);
-  const float c = fminf(fmaxf(t.r, lo), hi);
-  t.pg = -fminf(t.r * A, c * A);
+  t.r = r;
+  const float c = fminf(fmaxf(r, lo), hi);
+  const float rr = delta > 0.f ? fminf(r, delta) : r;
+  const float u = rr * A, v = c * A;
+  t.pg = -fminf(u, v);
   t.d = rf - lp;
   t.kl = expm1f(t.d) - t.d;  // exp(d) - d - 1
-  t.act = A >= 0.f ? (t.r <= hi) : (t.r >= lo);
+  t.act = (u <= v) ? (delta <= 0.f || r <= delta) : (r >= lo && r <= hi);
   return t;
+}
+
+// Sequence s's tokens [b, e): mean active log-ratio (lane-strided partial sums
+// in token order, then a xor butterfly) and active count.  The same code runs
+// wherever the sequence sits in the batch, so the bits do not depend on it.
+__device__ __forceinline__ void seq_log_ratio(const GrpoP& p, int b, int e, int lane, float& lr, int& n) {
+  float acc = 0.f;
+  int cnt = 0;
+  for (int i = b + lane; i < e; i += 32) {
+    if (!p.mask[i]) continue;
+    acc += p.logp[i] - p.old_logp[i];
+    cnt += 1;
+  }
+  acc = wsum(acc);
+  cnt = wsum_i(cnt);
+  n = cnt;
+  lr = cnt > 0 ? acc / static_cast<float>(cnt) : 0.f;
+}
+
+// Normaliser and (loss, policy, kl) from per-sequence totals, summed over
+// sequences in index order (lane-strided, then a xor butterfly).  Run by one
+// warp; shared by the single-call loss and by grpo_loss_from_sequence_totals so
+// that a batch split across data-parallel ranks reduces to the same bits.
+// Returns the per-token weight scale (1/T, 1/L or 1/C) and sets *flag when
+// the normaliser is zero.
+__device__ __forceinline__ float grpo_reduce_warp(const float* sP, const float* sK, const int* sN, int num_seqs,
+                                                  int reduction, double norm, float beta, int lane, float* loss3,
+                                                  int* status, int* flag_out) {
+  long long tot = 0;
+  int live = 0;
+  for (int s = lane; s < num_seqs; s += 32) {
+    tot += sN[s];
+    live += sN[s] > 0 ? 1 : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    live += __shfl_xor_sync(0xffffffffu, live, o);
+  }
+  float scale = 0.f;
+  int flag = 0;
+  if (reduction == GH_TOKEN_MEAN) {
+    const double den = norm > 0.0 ? norm : static_cast<double>(tot);
+    if (den > 0.0)
+      scale = static_cast<float>(1.0 / den);
+    else
+      flag = 1;
+  } else if (reduction == GH_SEQ_MEAN) {
+    const double den = norm > 0.0 ? norm : static_cast<double>(live);
+    if (den > 0.0)
+      scale = static_cast<float>(1.0 / den);
+    else
+      flag = 1;
+  } else {
+    scale = static_cast<float>(1.0 / norm);
+  }
+  float pol = 0.f, kl = 0.f;
+  if (!flag) {
+    for (int s = lane; s < num_seqs; s += 32) {
+      float w = scale;
+      if (reduction == GH_SEQ_MEAN) w = sN[s] > 0 ? scale / static_cast<float>(sN[s]) : 0.f;
+      pol += sP[s] * w;
+      kl += sK[s] * w;
+    }
+    pol = wsum(pol);
+    kl = wsum(kl);
+  }
+  if (lane == 0) {
+    if (flag && status) atomicOr(status, GH_DEV_NO_ACTIVE);
+    if (loss3) {
+      loss3[0] = pol + beta * kl;
+      loss3[1] = pol;
+      loss3[2] = kl;
+    }
+  }
+  *flag_out = flag;
+  return scale;
 }
 
 // one CTA of 1024 threads; dynamic shared memory: 3 * num_seqs words
@@ -109,7 +234,7 @@ __global__ void __launch_bounds__(1024) grpo_kernel(GrpoP p) {
   float* sP = sh;
   float* sK = sh + p.num_seqs;
   int* sN = reinterpret_cast<int*>(sh + 2 * p.num_seqs);
-  __shared__ float s_scale_tok;  // token_mean / fixed scale, or 1/L for seq_mean
+  __shared__ float s_scale;
   __shared__ int s_flag;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nw = blockDim.x >> 5;
   const float lo = 1.f - p.eps_low, hi = 1.f + p.eps_high;
@@ -137,12 +262,20 @@ __global__ void __launch_bounds__(1024) grpo_kernel(GrpoP p) {
     const int b = lower_bound_i(p.seq_id, 0, p.N, s);
     const int e = lower_bound_i(p.seq_id, b, p.N, s + 1);
     const float A = p.adv[s];
+    float rs = 1.f;
+    if (p.seq_level) {
+      float lr;
+      int n;
+      seq_log_ratio(p, b, e, lane, lr, n);
+      rs = expf(lr);
+    }
     float ap = 0.f, ak = 0.f;
     int an = 0;
     for (int i = b + lane; i < e; i += 32) {
       if (!p.mask[i]) continue;
       const float lp = p.logp[i];
-      const TokTerms tt = grpo_terms(lp, p.old_logp[i], p.ref_logp ? p.ref_logp[i] : lp, A, lo, hi);
+      const float r = p.seq_level ? rs : expf(lp - p.old_logp[i]);
+      const TokTerms tt = grpo_terms(r, lp, p.ref_logp ? p.ref_logp[i] : lp, A, lo, hi, p.delta);
       ap += tt.pg;
       ak += tt.kl;
       an += 1;
@@ -155,81 +288,76 @@ __global__ void __launch_bounds__(1024) grpo_kernel(GrpoP p) {
       sP[s] = ap;
       sK[s] = ak;
       sN[s] = an;
+      if (p.seq_policy) p.seq_policy[s] = ap;
+      if (p.seq_kl) p.seq_kl[s] = ak;
+      if (p.seq_count) p.seq_count[s] = an;
     }
   }
   if (nonfinite) atomicOr(p.status, GH_DEV_NONFINITE);
   __syncthreads();
 
-  // phase 2 (warp 0): normaliser, then policy/kl = sum_s total_s * scale_s in sequence order
+  // phase 2 (warp 0): normaliser, then (loss, policy, kl)
   if (warp == 0) {
-    long long tot = 0;
-    int live = 0;
-    for (int s = lane; s < p.num_seqs; s += 32) {
-      tot += sN[s];
-      live += sN[s] > 0 ? 1 : 0;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      tot += __shfl_xor_sync(0xffffffffu, tot, o);
-      live += __shfl_xor_sync(0xffffffffu, live, o);
-    }
-    float scale = 0.f;
-    int flag = 0;
-    if (p.reduction == GH_TOKEN_MEAN) {
-      const double den = p.norm > 0.0 ? p.norm : static_cast<double>(tot);
-      if (den > 0.0)
-        scale = static_cast<float>(1.0 / den);
-      else
-        flag = 1;
-    } else if (p.reduction == GH_SEQ_MEAN) {
-      const double den = p.norm > 0.0 ? p.norm : static_cast<double>(live);
-      if (den > 0.0)
-        scale = static_cast<float>(1.0 / den);
-      else
-        flag = 1;
-    } else {
-      scale = static_cast<float>(1.0 / p.norm);
-    }
-    float pol = 0.f, kl = 0.f;
-    if (!flag) {
-      for (int s = lane; s < p.num_seqs; s += 32) {
-        float w = scale;
-        if (p.reduction == GH_SEQ_MEAN) w = sN[s] > 0 ? scale / static_cast<float>(sN[s]) : 0.f;
-        pol += sP[s] * w;
-        kl += sK[s] * w;
-      }
-      pol = wsum(pol);
-      kl = wsum(kl);
-    }
+    int flag;
+    const float scale = grpo_reduce_warp(sP, sK, sN, p.num_seqs, p.reduction, p.norm, p.beta, lane, p.loss3,
+                                         p.status, &flag);
     if (lane == 0) {
-      s_scale_tok = scale;
+      s_scale = scale;
       s_flag = flag;
-      if (flag) atomicOr(p.status, GH_DEV_NO_ACTIVE);
-      if (p.loss3) {
-        p.loss3[0] = pol + p.beta * kl;
-        p.loss3[1] = pol;
-        p.loss3[2] = kl;
-      }
     }
   }
   __syncthreads();
 
-  // phase 3: coef_i = w_i (-A r act + beta (1 - exp(d)))
+  // phase 3 (warp per sequence): coef_i = w_i (-A r act + beta (1 - exp(d)));
+  // at the sequence level r and act are the sequence's (every token of a
+  // sequence has the same weight, so the gradient of the shared ratio lands
+  // on each token with that weight)
   if (p.coef) {
-    const float scale = s_scale_tok;
+    const float scale = s_scale;
     const int flag = s_flag;
-    for (int i = t; i < p.N; i += blockDim.x) {
-      float c = 0.f;
-      if (p.mask[i] && !flag) {
-        const int s = p.seq_id[i];
+    for (int i = t; i < p.N; i += blockDim.x)
+      if (!p.mask[i] || flag) p.coef[i] = 0.f;
+    if (!flag) {
+      for (int s = warp; s < p.num_seqs; s += nw) {
+        const int b = lower_bound_i(p.seq_id, 0, p.N, s);
+        const int e = lower_bound_i(p.seq_id, b, p.N, s + 1);
         const float A = p.adv[s];
-        const float lp = p.logp[i];
-        const TokTerms tt = grpo_terms(lp, p.old_logp[i], p.ref_logp ? p.ref_logp[i] : lp, A, lo, hi);
-        const float w = p.reduction == GH_SEQ_MEAN ? scale / static_cast<float>(sN[s]) : scale;
-        c = w * (-A * tt.r * (tt.act ? 1.f : 0.f) - p.beta * expm1f(tt.d));
+        float rs = 1.f;
+        if (p.seq_level) {
+          float lr;
+          int n;
+          seq_log_ratio(p, b, e, lane, lr, n);
+          rs = expf(lr);
+        }
+        const float w = p.reduction == GH_SEQ_MEAN ? (sN[s] > 0 ? scale / static_cast<float>(sN[s]) : 0.f) : scale;
+        for (int i = b + lane; i < e; i += 32) {
+          if (!p.mask[i]) continue;
+          const float lp = p.logp[i];
+          const float r = p.seq_level ? rs : expf(lp - p.old_logp[i]);
+          const TokTerms tt = grpo_terms(r, lp, p.ref_logp ? p.ref_logp[i] : lp, A, lo, hi, p.delta);
+          p.coef[i] = w * (-A * tt.r * (tt.act ? 1.f : 0.f) - p.beta * expm1f(tt.d));
+        }
       }
-      p.coef[i] = c;
     }
+  }
+}
+
+// loss from gathered per-sequence totals (one warp; dynamic shared memory 3 * num_seqs)
+__global__ void grpo_totals_kernel(int num_seqs, const float* seq_policy, const float* seq_kl, const int* seq_count,
+                                   int reduction, double norm, float beta, float* loss3, int* status) {
+  extern __shared__ float sh[];
+  float* sP = sh;
+  float* sK = sh + num_seqs;
+  int* sN = reinterpret_cast<int*>(sh + 2 * num_seqs);
+  for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+    sP[s] = seq_policy[s];
+    sK[s] = seq_kl[s];
+    sN[s] = seq_count[s];
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int flag;
+    grpo_reduce_warp(sP, sK, sN, num_seqs, reduction, norm, beta, threadIdx.x, loss3, status, &flag);
   }
 }
 
@@ -411,6 +539,15 @@ cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const fl
   return cudaGetLastError();
 }
 
+cudaError_t launch_merge_shards(int N, int V_total, int splits, const float* part_m, const float* part_s,
+                                const float* zy, const ShardBounds& sb, const int32_t* targets, const uint8_t* mask,
+                                float* logp, float* lse, int* status, cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  merge_shards_kernel<<<static_cast<unsigned>(ceil_div(N, 256)), 256, 0, st>>>(N, V_total, splits, part_m, part_s, zy,
+                                                                                sb, targets, mask, logp, lse, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_grpo* g, float* coef, float* loss3,
                         int* status, cudaStream_t st) {
   GrpoP p;
@@ -426,9 +563,14 @@ cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_
   p.eps_low = g->eps_low;
   p.eps_high = g->eps_high;
   p.beta = g->beta;
+  p.delta = g->delta;
+  p.seq_level = g->ratio_level;
   p.norm = g->norm;
   p.coef = coef;
   p.loss3 = loss3;
+  p.seq_policy = g->seq_policy;
+  p.seq_kl = g->seq_kl;
+  p.seq_count = g->seq_count;
   p.status = status;
   const size_t sm = static_cast<size_t>(3) * g->num_seqs * sizeof(float);
   static bool attr = false;
@@ -439,6 +581,20 @@ cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_
     attr = true;
   }
   grpo_kernel<<<1, 1024, sm, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grpo_totals(int num_seqs, const float* seq_policy, const float* seq_kl, const int32_t* seq_count,
+                               int reduction, double norm, float beta, float* loss3, int* status, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(grpo_totals_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         3 * MAX_SEQS * static_cast<int>(sizeof(float)));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  grpo_totals_kernel<<<1, 256, static_cast<size_t>(3) * num_seqs * sizeof(float), st>>>(
+      num_seqs, seq_policy, seq_kl, seq_count, reduction, norm, beta, loss3, status);
   return cudaGetLastError();
 }
 

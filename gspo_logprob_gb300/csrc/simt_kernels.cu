@@ -71,7 +71,8 @@ __device__ __forceinline__ void f32_logits_tile(const float* __restrict__ H, con
 // sub-blocks and, for each, the split's vocabulary tiles in order.
 __global__ void __launch_bounds__(F_THREADS) f32_fwd_kernel(const float* __restrict__ H, const float* __restrict__ W,
                                                            const int* __restrict__ targets, int N, int D, int V,
-                                                           int row_tile, float* part_m, float* part_s, float* zy) {
+                                                           int row_tile, int col_offset, float* part_m,
+                                                           float* part_s, float* zy) {
   __shared__ float Hs[F_ROWS][F_KC];
   __shared__ float Ws[256][F_KC + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(F_THREADS) f32_fwd_kernel(const float* __restr
       m[r] = -INFINITY;
       s[r] = 0.f;
       const int gr = r0 + warp * 4 + r;
-      y[r] = gr < N ? targets[gr] : -1;
+      y[r] = gr < N ? targets[gr] - col_offset : -1;  // local column of the target
     }
     for (int vt = t_begin; vt < t_end; ++vt) {
       const int c0 = vt * 256;
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(F_THREADS) f32_dlogits_kernel(const float* __r
                                                                const float* __restrict__ lse,
                                                                const float* __restrict__ coef,
                                                                const float* __restrict__ grad_out, int N, int D,
-                                                               int V, int vb0, int ldg, float* G) {
+                                                               int V, int vb0, int ldg, int col_offset, float* G) {
   __shared__ float Hs[F_ROWS][F_KC];
   __shared__ float Ws[256][F_KC + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(F_THREADS) f32_dlogits_kernel(const float* __r
     if (gr >= N) continue;
     const float sc = g * coef[gr];
     const float L = lse[gr];
-    const int y = targets[gr];
+    const int y = targets[gr] - col_offset;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int col = c0 + lane + 32 * j;
@@ -235,7 +236,8 @@ cudaError_t launch_fwd_f32(const F32FwdArgs& a, cudaStream_t st) {
   const int splits = static_cast<int>(ceil_div(ceil_div(a.V, VTILE), TILES_PER_SPLIT));
   dim3 grid(static_cast<unsigned>(ceil_div(a.N, rt)), static_cast<unsigned>(splits));
   if (a.N <= 0) return cudaSuccess;
-  f32_fwd_kernel<<<grid, F_THREADS, 0, st>>>(a.H, a.W, a.targets, a.N, a.D, a.V, rt, a.part_m, a.part_s, a.zy);
+  f32_fwd_kernel<<<grid, F_THREADS, 0, st>>>(a.H, a.W, a.targets, a.N, a.D, a.V, rt, a.col_offset, a.part_m, a.part_s,
+                                              a.zy);
   return cudaGetLastError();
 }
 
@@ -243,7 +245,7 @@ cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st) {
   dim3 grid(static_cast<unsigned>(ceil_div(a.N, F_ROWS)), static_cast<unsigned>(ceil_div(a.width, 256)));
   if (a.N <= 0) return cudaSuccess;
   f32_dlogits_kernel<<<grid, F_THREADS, 0, st>>>(a.H, a.W, a.targets, a.lse, a.coef, a.grad_out, a.N, a.D, a.V,
-                                                  a.vb0, a.ldg, a.G);
+                                                  a.vb0, a.ldg, a.col_offset, a.G);
   return cudaGetLastError();
 }
 

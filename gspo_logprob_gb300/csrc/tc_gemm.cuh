@@ -304,6 +304,7 @@ struct EpiFwdLse {
     float* part_s;  // [splits, N]
     float* zy;      // [N]
     const int* targets;
+    int col_offset;  // global vocabulary id of local column 0 (vocabulary shards)
   };
   float m, s;
   int y, grow;
@@ -314,7 +315,7 @@ struct EpiFwdLse {
     s = 0.f;
     grow = m_blk * sc.m_step + row;
     valid = row < sc.m_step && grow < p.N;
-    y = valid ? __ldg(p.targets + grow) : -1;
+    y = valid ? __ldg(p.targets + grow) - p.col_offset : -1;  // local column of the target
   }
 
   __device__ __forceinline__ void tile(const Params& p, const TcSched&, uint32_t taddr, int, int n_blk, int) {
@@ -330,7 +331,7 @@ struct EpiFwdLse {
         float z = 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) z = (j == rel) ? v[j] : z;
-        p.zy[grow] = z;  // yy >= 0 only for valid rows
+        p.zy[grow] = z;  // rel in [0, 32) only for valid rows
       }
       if (col0 + 32 > p.V) {
 #pragma unroll
@@ -383,6 +384,7 @@ struct EpiDlogits {
     const float* coef;
     const float* grad_out;  // device scalar or nullptr (1)
     const int* targets;
+    int col_offset;  // global vocabulary id of local column 0 (vocabulary shards)
     __nv_bfloat16* G;
   };
   __device__ __forceinline__ void begin_task(const Params&, const TcSched&, int, int) {}
@@ -395,7 +397,7 @@ struct EpiDlogits {
     const float g = p.grad_out ? __ldg(p.grad_out) : 1.f;
     const float scale = valid ? g * __ldg(p.coef + grow) : 0.f;
     const float lse2 = valid ? __ldg(p.lse + grow) * LOG2E : 0.f;
-    const int yy = valid ? __ldg(p.targets + grow) : -1;
+    const int yy = valid ? __ldg(p.targets + grow) - p.col_offset : -1;
 #pragma unroll 1
     for (int c = 0; c < TC_BN / 32; ++c) {
       float v[32];

@@ -99,6 +99,7 @@ cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st) {
   ep.part_s = a.part_s;
   ep.zy = a.zy;
   ep.targets = a.targets;
+  ep.col_offset = a.col_offset;
   // every row tile of a split before the next split: the split's W tiles are
   // shared in L2 by all CTAs working on it
   if (a.row_tile == 64 || a.row_tile == 128) {
@@ -125,6 +126,7 @@ cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st) {
   ep.coef = a.coef;
   ep.grad_out = a.grad_out;
   ep.targets = a.targets;
+  ep.col_offset = a.col_offset;
   ep.G = static_cast<__nv_bfloat16*>(a.G);
   const int nkb = static_cast<int>(ceil_div(a.D, TC_BK));
   const int nn = static_cast<int>(ceil_div(a.width, TC_BN));

@@ -108,10 +108,14 @@ def raise_on_status(status: torch.Tensor, allow: int = 0) -> int:
 
 def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=None, seq_id=None,
                       num_seqs: int = 0, eps_low: float = 0.2, eps_high: float = 0.2, beta: float = 0.0,
-                      reduction: str = "token_mean", norm: float = 0.0, row_tile: int = 0,
+                      reduction: str = "token_mean", norm: float = 0.0, delta: float = 0.0,
+                      ratio_level: str = "token", seq_totals: bool = False, row_tile: int = 0,
                       want_coef: bool = True, status: Optional[torch.Tensor] = None, out: Optional[dict] = None):
     """Selected-token log-probs and LSE; with ``old_logp`` given, also the GRPO
-    loss (loss, policy_loss, kl) and coef = d loss / d logp.
+    loss (loss, policy_loss, kl) and coef = d loss / d logp.  ``delta`` > 0
+    caps the unclipped ratio (two-sided clip); ``ratio_level="sequence"`` uses
+    one ratio per sequence; ``seq_totals`` also returns the per-sequence totals
+    (seq_policy, seq_kl, seq_count) for a data-parallel reduction.
 
     Returns a dict with logp, lse, and (GRPO) coef, loss3, plus status."""
     head = make_head(H, W, targets, mask, row_tile)
@@ -130,10 +134,18 @@ def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=
         _need(adv, "adv", _F32)
         _need(seq_id, "seq_id", torch.int32, (N,))
         num_seqs = int(num_seqs or adv.numel())
+        totals = None
+        if seq_totals:
+            totals = (torch.empty(num_seqs, dtype=_F32, device=dev), torch.empty(num_seqs, dtype=_F32, device=dev),
+                      torch.empty(num_seqs, dtype=torch.int32, device=dev))
+            out.update(seq_policy=totals[0], seq_kl=totals[1], seq_count=totals[2])
         g = GhGrpo(old_logp=old_logp.data_ptr(), ref_logp=ref_logp.data_ptr() if ref_logp is not None else None,
                    adv=adv.data_ptr(), seq_id=seq_id.data_ptr(), num_seqs=num_seqs,
                    reduction=_abi.REDUCTIONS[reduction], eps_low=eps_low, eps_high=eps_high, beta=beta,
-                   reserved=0.0, norm=float(norm))
+                   delta=float(delta), norm=float(norm), ratio_level=_abi.RATIO_LEVELS[ratio_level], reserved=0,
+                   seq_policy=totals[0].data_ptr() if totals else None,
+                   seq_kl=totals[1].data_ptr() if totals else None,
+                   seq_count=totals[2].data_ptr() if totals else None)
         if want_coef:
             coef = out.get("coef") if out.get("coef") is not None else torch.empty(N, dtype=_F32, device=dev)
         loss3 = out.get("loss3") if out.get("loss3") is not None else torch.empty(3, dtype=_F32, device=dev)
@@ -144,6 +156,78 @@ def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=
     _abi.check(code, "grpo_head_forward")
     out.update(logp=logp, lse=lse, coef=coef, loss3=loss3, status=st)
     return out
+
+
+def vocab_shard_bounds(V_total: int, num_shards: int):
+    """[(start, length)] of each vocabulary shard: whole 1024-column splits,
+    the remainder spread over the first shards (host-only library call)."""
+    lib = _lib()
+    out = []
+    for r in range(num_shards):
+        st, ln = ctypes.c_int64(), ctypes.c_int64()
+        _abi.check(lib.gh_vocab_shard_bounds(int(V_total), int(num_shards), r, ctypes.byref(st), ctypes.byref(ln)),
+                   "gh_vocab_shard_bounds")
+        out.append((int(st.value), int(ln.value)))
+    return out
+
+
+def grpo_head_logprob_shard(H, W_shard, targets, mask, *, vocab_start: int, V_total: int, row_tile: int = 0,
+                            status: Optional[torch.Tensor] = None):
+    """One vocabulary shard's split partials (part_m, part_s [S_shard, N]) and
+    the target logits of the rows whose target lies in the shard (zy [N])."""
+    head = make_head(H, W_shard, targets, mask, row_tile)
+    dev = H.device
+    N = head.N
+    splits = -(-(-(-head.V // 256)) // 4)
+    part_m = torch.empty(splits, N, dtype=_F32, device=dev)
+    part_s = torch.empty(splits, N, dtype=_F32, device=dev)
+    zy = torch.zeros(N, dtype=_F32, device=dev)
+    st = new_status(dev) if status is None else status
+    code = _lib().grpo_head_logprob_shard(ctypes.byref(head), int(vocab_start), int(V_total), _ptr(part_m),
+                                          _ptr(part_s), _ptr(zy), _ptr(st), _stream(dev))
+    _abi.check(code, "grpo_head_logprob_shard")
+    return dict(part_m=part_m, part_s=part_s, zy=zy, status=st)
+
+
+def grpo_logprob_merge(part_m, part_s, zy, shard_starts, targets, mask, *, V_total: int,
+                       status: Optional[torch.Tensor] = None):
+    """logp, lse [N] from the gathered shard partials (concatenated in shard
+    order) and the shards' zy rows [num_shards, N]; shard_starts has
+    num_shards + 1 host integers."""
+    S, N = part_m.shape
+    _need(part_m, "part_m", _F32)
+    _need(part_s, "part_s", _F32, (S, N))
+    num_shards = len(shard_starts) - 1
+    _need(zy, "zy", _F32, (num_shards, N))
+    _need(targets, "targets", torch.int32, (N,))
+    _need(mask, "mask", torch.uint8, (N,))
+    dev = part_m.device
+    logp = torch.empty(N, dtype=_F32, device=dev)
+    lse = torch.empty(N, dtype=_F32, device=dev)
+    st = new_status(dev) if status is None else status
+    starts = (ctypes.c_int64 * (num_shards + 1))(*[int(x) for x in shard_starts])
+    code = _lib().grpo_logprob_merge(N, int(V_total), num_shards, starts, _ptr(part_m), _ptr(part_s), _ptr(zy),
+                                     _ptr(targets), _ptr(mask), _ptr(logp), _ptr(lse), _ptr(st), _stream(dev))
+    _abi.check(code, "grpo_logprob_merge")
+    return dict(logp=logp, lse=lse, status=st)
+
+
+def grpo_loss_from_sequence_totals(seq_policy, seq_kl, seq_count, *, reduction: str = "token_mean",
+                                   norm: float = 0.0, beta: float = 0.0, status: Optional[torch.Tensor] = None):
+    """(loss, policy_loss, kl) from per-sequence totals gathered in global
+    sequence order (bitwise equal to a single forward over the whole batch)."""
+    S = seq_policy.numel()
+    _need(seq_policy, "seq_policy", _F32, (S,))
+    _need(seq_kl, "seq_kl", _F32, (S,))
+    _need(seq_count, "seq_count", torch.int32, (S,))
+    dev = seq_policy.device
+    loss3 = torch.empty(3, dtype=_F32, device=dev)
+    st = new_status(dev) if status is None else status
+    code = _lib().grpo_loss_from_sequence_totals(S, _ptr(seq_policy), _ptr(seq_kl), _ptr(seq_count),
+                                                 _abi.REDUCTIONS[reduction], float(norm), float(beta), _ptr(loss3),
+                                                 _ptr(st), _stream(dev))
+    _abi.check(code, "grpo_loss_from_sequence_totals")
+    return dict(loss3=loss3, status=st)
 
 
 def gspo_segment_loss(logp, old_logp, mask, seg_id, num_segments: int, seg_adv, *, eps_low: float,

@@ -102,10 +102,20 @@ typedef struct {
   float eps_low;          /* ratio clipped to [1 - eps_low, 1 + eps_high]                 */
   float eps_high;
   float beta;             /* weight of the k3 KL term exp(d) - d - 1, d = ref - logp      */
-  float reserved;         /* must be 0                                                    */
+  float delta;            /* > 0: two-sided clip, the unclipped ratio is capped at delta
+                             (Liger-Kernel PR #1160, Testing Done: the delta parameter);
+                             0: off                                                      */
   double norm;            /* > 0: explicit normaliser (T, L or C above, e.g. the active
-                             token count of the whole step across micro-batches); 0: from
-                             this call (token/seq mean only)                             */
+                             token count of the whole step across micro-batches or
+                             data-parallel ranks); 0: from this call (token/seq mean)   */
+  int32_t ratio_level;    /* 0: token ratios exp(logp - old); 1: one ratio per sequence,
+                             exp of the mean active log-ratio of the sequence (the
+                             "sequence" importance-sampling level of the same tests)    */
+  int32_t reserved;       /* must be 0                                                    */
+  float* seq_policy;      /* optional out [num_seqs]: sum over the sequence's active
+                             tokens of the policy term (before the normaliser)           */
+  float* seq_kl;          /* optional out [num_seqs]: same for the KL term               */
+  int32_t* seq_count;     /* optional out [num_seqs]: active tokens of each sequence     */
 } gh_grpo;
 
 /* Bytes of scratch `ws` grpo_head_forward needs for this problem. */
@@ -120,8 +130,10 @@ size_t grpo_head_backward_workspace_size(const gh_head* head);
  *         out-of-range target, 0 for an inactive one).
  *   lse   [N] fp32 out: LSE_i over the real vocabulary.
  *   coef  [N] fp32 out (may be NULL; needs grpo): coef_i = d loss / d logp_i =
- *         w_i (-A_s r_i act_i + beta (1 - exp(ref_i - logp_i))), with
- *         r = exp(logp - old), act = 1 where the unclipped PPO term is the min.
+ *         w_i (-A_s r_i act_i + beta (1 - exp(ref_i - logp_i))), with r the
+ *         token (or sequence) ratio and act = 1 where the PPO term moving with
+ *         r is the minimum: the unclipped term below the delta cap, or the
+ *         clipped term inside the clip band.
  *   loss3 [3] fp32 out (may be NULL; needs grpo): (loss, policy_loss, kl) with
  *         loss = policy_loss + beta kl, summed per sequence first and then over
  *         sequences in index order.
@@ -131,6 +143,59 @@ size_t grpo_head_backward_workspace_size(const gh_head* head);
 gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* logp, float* lse,
                             float* coef, float* loss3, int32_t* status, void* ws, size_t ws_bytes,
                             void* stream);
+
+/*
+ * Vocabulary-parallel (tensor-parallel) log-prob, RL-Kernel PR #291, PR
+ * description: each rank holds a vocabulary shard of W; padded columns are
+ * masked before the local (max, sumexp) partials; partials are moved by
+ * all-gather and merged in fixed global shard order; cross-degree bitwise
+ * equality needs a tile decomposition that does not depend on the number of
+ * shards.  Here the decomposition is the global grid of 1024-column splits:
+ * shard bounds are multiples of 1024 (gh_vocab_shard_bounds gives an even
+ * split), every shard's splits are global splits, and the merged result is
+ * bitwise the one grpo_head_forward gives on the whole vocabulary.
+ *
+ * gh_vocab_shard_bounds: columns [*start, *start + *len) of shard `rank` of
+ * `num_shards` over V_total (whole splits, the remainder spread over the first
+ * shards; num_shards <= ceil(V_total / 1024)).  Host only.
+ */
+gh_status gh_vocab_shard_bounds(int64_t V_total, int32_t num_shards, int32_t rank, int64_t* start, int64_t* len);
+
+/*
+ * One rank's shard: head->W is the shard [head->V, D] holding global columns
+ * [vocab_start, vocab_start + head->V) of V_total; targets are global ids.
+ * Writes the shard's split partials part_m, part_s [S_shard, N] fp32
+ * (S_shard = ceil(ceil(head->V / 256) / 4)) and zy [N] = z_{i, y_i} for the
+ * rows whose target lies in the shard (other rows untouched).  vocab_start
+ * must be a multiple of 1024 and every shard but the last whole splits.
+ */
+gh_status grpo_head_logprob_shard(const gh_head* head, int64_t vocab_start, int64_t V_total, float* part_m,
+                                  float* part_s, float* zy, int32_t* status, void* stream);
+
+/*
+ * Merge of the gathered shard outputs: part_m, part_s [S_total, N] are the
+ * shards' partials concatenated in shard order (= global split order), zy
+ * [num_shards, N] their zy rows, shard_starts (HOST array, num_shards + 1
+ * entries) the bounds.  Writes logp and lse [N] exactly as grpo_head_forward.
+ */
+gh_status grpo_logprob_merge(int64_t N, int64_t V_total, int32_t num_shards, const int64_t* shard_starts,
+                             const float* part_m, const float* part_s, const float* zy, const int32_t* targets,
+                             const uint8_t* mask, float* logp, float* lse, int32_t* status, void* stream);
+
+/*
+ * (loss, policy_loss, kl) from per-sequence totals gathered across
+ * data-parallel ranks (RL-Kernel PR #291, Key Changes: Reference Op: each rank
+ * owns whole sequences; per-sequence totals are all-gathered as a
+ * [num_sequences] vector and summed in sequence order, never all-reduced).
+ * seq_policy, seq_kl [num_seqs] fp32 and seq_count [num_seqs] int32 are the
+ * concatenation, in global sequence order, of the gh_grpo.seq_* outputs of
+ * every rank's grpo_head_forward; the sum runs in the same order and code as
+ * a single-call forward over the whole batch, so the result is bitwise the
+ * same as that call's loss3.  `norm` as in gh_grpo.  loss3 [3] out.
+ */
+gh_status grpo_loss_from_sequence_totals(int32_t num_seqs, const float* seq_policy, const float* seq_kl,
+                                         const int32_t* seq_count, int32_t reduction, double norm, float beta,
+                                         float* loss3, int32_t* status, void* stream);
 
 /*
  * GSPO sequence-level loss over packed documents (Fast-LLM PR #554, What):
@@ -212,9 +277,9 @@ int32_t gh_abi_version(void);
  * the recorded events).  gh_launch_count counts all launches since load.
  * Kinds: 0 fwd logits+LSE, 1 merge, 2 GRPO loss, 3 GSPO loss, 4 dlogits,
  * 5 dH GEMM, 6 dW GEMM, 7 advantage, 8 fp32 forward, 9 fp32 dlogits,
- * 10 fp32 GEMM, 11 timeout probe.
+ * 10 fp32 GEMM, 11 timeout probe, 12 GRPO loss from sequence totals, 13 shard merge.
  */
-#define GH_NUM_KERNEL_KINDS 12
+#define GH_NUM_KERNEL_KINDS 14
 void gh_profile_enable(int32_t on);
 void gh_profile_reset(void);
 gh_status gh_profile_read(int32_t kind, int64_t* launches, double* total_ms);

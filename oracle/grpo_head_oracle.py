@@ -23,7 +23,10 @@ Pins (tests/test_oracle_*.py):
   group_advantages : numpy mean/std(ddof=1) of each group, zero-spread groups
   grpo_loss : ratio==1 & beta=0 closed form, clip-free band, k3 >= 0 and 0 at
       equality, reductions coincide on equal lengths, worked example fixture,
-      finite differences of the loss w.r.t. logp
+      finite differences of the loss w.r.t. logp (token and sequence ratios,
+      with and without the two-sided cap), the cap's worked example, a cap
+      above every ratio changes nothing, one-token sequences and constant
+      per-sequence log-ratios reduce the sequence level to the token level
   gspo_loss : length-1 segments reduce to token PPO-clip, one segment closed
       form, np.bincount counts, finite differences w.r.t. logp
   dlogits / head_backward : finite differences of the loss w.r.t. H and W,
@@ -172,26 +175,38 @@ def group_advantages(rewards: np.ndarray, group_size: int, eps: float = 1e-4) ->
 REDUCTIONS = ("token_mean", "seq_mean", "fixed")
 
 
-def _token_terms(logp, old, ref, A_tok, eps_low, eps_high):
+def _token_terms(logp, old, ref, A_tok, eps_low, eps_high, delta=0.0, log_ratio=None):
     """Per-token PPO-clip surrogate and k3 KL ([RLK] "Overview": ratio,
     clipping and reference KL act per token).
 
-    r = exp(logp - old); c = clip(r, 1-eps_low, 1+eps_high);
-    pg = -min(r A, c A); d = ref - logp; kl = exp(d) - d - 1;
-    act = 1 where the unclipped term is the minimum (ties count as unclipped),
-    i.e. d pg / d logp = -A r act."""
-    r = np.exp(logp - old)
+    r = exp(logp - old) (or exp(log_ratio) when given: the sequence-level
+    ratio); c = clip(r, 1-eps_low, 1+eps_high); with the two-sided clip
+    ([Liger] test parameter delta) the unclipped ratio is capped at delta:
+    u = min(r, delta) A, else u = r A; v = c A; pg = -min(u, v);
+    d = ref - logp; kl = exp(d) - d - 1.  d pg / d log r = -A r act with
+    act = 1 when the unclipped term is the minimum (ties count as unclipped)
+    and the cap does not bind (r <= delta), or when the clipped term is the
+    minimum and r lies inside the clip band; act = 0 otherwise."""
+    r = np.exp(logp - old) if log_ratio is None else np.exp(log_ratio)
     c = np.clip(r, 1.0 - eps_low, 1.0 + eps_high)
-    pg = -np.minimum(r * A_tok, c * A_tok)
+    rr = np.minimum(r, delta) if delta > 0 else r
+    u = rr * A_tok
+    v = c * A_tok
+    pg = -np.minimum(u, v)
     d = ref - logp
     kl = np.exp(d) - d - 1.0
-    act = np.where(A_tok >= 0, r <= 1.0 + eps_high, r >= 1.0 - eps_low).astype(np.float64)
-    return r, pg, kl, act, d
+    # the gradient follows the active branch: the unclipped (capped) term
+    # moves with r unless the cap binds; the clipped term moves with r only
+    # inside the clip band (where clip(r) = r)
+    in_band = (r >= 1.0 - eps_low) & (r <= 1.0 + eps_high)
+    below_cap = (r <= delta) if delta > 0 else np.ones_like(r, dtype=bool)
+    act = np.where(u <= v, below_cap, in_band)
+    return r, pg, kl, act.astype(np.float64), d
 
 
 def grpo_loss(logp, old, ref, mask, seq_id, adv, num_seqs: int, eps_low: float,
               eps_high: float, beta: float, reduction: str = "token_mean",
-              norm: float = 0.0):
+              norm: float = 0.0, delta: float = 0.0, ratio_level: str = "token"):
     """Masked GRPO loss, its (policy, kl) parts and d loss / d logp.
 
     Reductions ([RLK] "Key Changes: Loss Contract", token_normalizer):
@@ -207,9 +222,18 @@ def grpo_loss(logp, old, ref, mask, seq_id, adv, num_seqs: int, eps_low: float,
     (loss, policy_loss, kl)).  With no active tokens token_mean and
     seq_mean raise (review note on the zero-active-token guard), fixed gives 0.
 
-    coef_i = d loss / d logp_i = w_i (-A_s r_i act_i + beta (1 - exp(ref_i - logp_i)))."""
+    ``delta`` > 0 caps the unclipped ratio ([Liger] "Testing Done": the
+    two-sided clip parameter, 2.0 in the failing cases).  ``ratio_level`` =
+    "sequence" uses one ratio per sequence, exp of the mean active log-ratio
+    of the sequence ([Liger] "Testing Done": the "sequence" importance
+    sampling level), for every token of the sequence; the KL stays per token.
+
+    coef_j = d loss / d logp_j; token level: w_j (-A_s r_j act_j + beta (1 - e^{d_j}));
+    sequence level: w_j beta (1 - e^{d_j}) + (m_j / n_s) sum_{i in s} w_i (-A_s r_s act_s)."""
     if reduction not in REDUCTIONS:
         raise OracleError(reduction)
+    if ratio_level not in ("token", "sequence"):
+        raise OracleError(ratio_level)
     logp = np.asarray(logp, dtype=np.float64)
     N = logp.shape[0]
     m = np.asarray(mask, dtype=np.float64)
@@ -220,18 +244,27 @@ def grpo_loss(logp, old, ref, mask, seq_id, adv, num_seqs: int, eps_low: float,
     lp = np.where(m > 0, logp, 0.0)
     od = np.where(m > 0, np.asarray(old, dtype=np.float64), 0.0)
     rf = np.where(m > 0, np.asarray(ref, dtype=np.float64), 0.0) if ref is not None else lp
-    r, pg, kl, act, d = _token_terms(lp, od, rf, A_tok, eps_low, eps_high)
+
+    # explicit loop: per-sequence active counts (and mean log-ratios)
+    n = np.zeros(num_seqs, dtype=np.int64)
+    lr_sum = np.zeros(num_seqs)
+    for i in range(N):
+        if m[i] > 0:
+            n[seq[i]] += 1
+            lr_sum[seq[i]] += lp[i] - od[i]
+    log_ratio = None
+    if ratio_level == "sequence":
+        seq_lr = np.where(n > 0, lr_sum / np.maximum(n, 1), 0.0)
+        log_ratio = np.where(m > 0, seq_lr[seq], 0.0)
+    r, pg, kl, act, d = _token_terms(lp, od, rf, A_tok, eps_low, eps_high, delta, log_ratio)
 
     # explicit loop: per-sequence totals in token order
     P = np.zeros(num_seqs)
     K = np.zeros(num_seqs)
-    n = np.zeros(num_seqs, dtype=np.int64)
     for i in range(N):
         if m[i] > 0:
-            s = seq[i]
-            P[s] += pg[i]
-            K[s] += kl[i]
-            n[s] += 1
+            P[seq[i]] += pg[i]
+            K[seq[i]] += kl[i]
 
     total = int(n.sum())
     live = int((n > 0).sum())
@@ -257,7 +290,16 @@ def grpo_loss(logp, old, ref, mask, seq_id, adv, num_seqs: int, eps_low: float,
         klsum += K[s] * seq_scale[s]
     loss = policy + beta * klsum
     w = m * seq_scale[seq]
-    coef = w * (-A_tok * r * act + beta * (1.0 - np.exp(d)))
+    if ratio_level == "token":
+        coef = w * (-A_tok * r * act + beta * (1.0 - np.exp(d)))
+    else:
+        wsum = np.zeros(num_seqs)
+        g = np.zeros(num_seqs)
+        for i in range(N):
+            if m[i] > 0:
+                wsum[seq[i]] += w[i]
+                g[seq[i]] = -A_tok[i] * r[i] * act[i]      # shared by the sequence
+        coef = w * beta * (1.0 - np.exp(d)) + (m / np.maximum(n[seq], 1)) * wsum[seq] * g[seq]
     coef = np.where(m > 0, coef, 0.0)
     abs_terms = float(np.sum(np.abs(w * (pg + beta * kl))))
     return dict(loss=loss, policy=policy, kl=klsum, coef=coef, per_seq_policy=P,

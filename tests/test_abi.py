@@ -47,19 +47,20 @@ def test_struct_layout_matches_c(lib, tmp_path):
     prog = tmp_path / "layout.c"
     prog.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "grpo_head.h"\n'
-        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(gh_head), offsetof(gh_head, H),"
-        " offsetof(gh_head, mask), sizeof(gh_grpo), offsetof(gh_grpo, num_seqs), offsetof(gh_grpo, norm));return 0;}\n")
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(gh_head), offsetof(gh_head, H),"
+        " offsetof(gh_head, mask), sizeof(gh_grpo), offsetof(gh_grpo, num_seqs), offsetof(gh_grpo, norm),"
+        " offsetof(gh_grpo, ratio_level), offsetof(gh_grpo, seq_count));return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run([gcc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(prog), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     from gspo_logprob_gb300._abi import GhGrpo, GhHead
     want = [ctypes.sizeof(GhHead), GhHead.H.offset, GhHead.mask.offset, ctypes.sizeof(GhGrpo),
-            GhGrpo.num_seqs.offset, GhGrpo.norm.offset]
+            GhGrpo.num_seqs.offset, GhGrpo.norm.offset, GhGrpo.ratio_level.offset, GhGrpo.seq_count.offset]
     assert got == want
 
 
 def test_host_only_calls(lib):
-    assert lib.gh_abi_version() == 100
+    assert lib.gh_abi_version() == 101
     assert lib.gh_status_string(0) == b"GH_OK"
     assert lib.gh_status_string(3) == b"GH_ERR_WORKSPACE"
     assert lib.gh_kernel_kind_name(0) == b"fwd_logits_lse_tc"
@@ -139,3 +140,29 @@ def test_gspo_and_advantage_validation(lib):
 def test_binding_imports_without_gpu():
     import gspo_logprob_gb300 as g
     assert callable(g.grpo_head_forward) and callable(g.grpo_head_backward)
+
+
+def test_vocab_shard_bounds(lib):
+    import gspo_logprob_gb300 as g
+    assert g.vocab_shard_bounds(5000, 2) == [(0, 3072), (3072, 1928)]
+    b = g.vocab_shard_bounds(151936, 4)   # 149 splits of 1024 -> 38, 37, 37, 37
+    assert b == [(0, 38912), (38912, 37888), (76800, 37888), (114688, 37248)]
+    for V, P in ((5000, 5), (151936, 7), (1, 1), (1025, 2)):
+        b = g.vocab_shard_bounds(V, P)
+        assert b[0][0] == 0 and sum(x[1] for x in b) == V
+        assert all(x[0] % 1024 == 0 for x in b)
+        assert all(b[i][0] + b[i][1] == b[i + 1][0] for i in range(P - 1))
+    st, ln = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.gh_vocab_shard_bounds(5000, 6, 0, ctypes.byref(st), ctypes.byref(ln)) == 1  # more shards than splits
+
+
+def test_shard_argument_validation(lib):
+    h = _head(N=100, D=64, V=3000)
+    # vocab_start not on the 1024-column split grid
+    assert lib.grpo_head_logprob_shard(ctypes.byref(h), 512, 5000, 0x100, 0x100, 0x100, 0x100, None) == 1
+    # a middle shard that is not whole splits
+    assert lib.grpo_head_logprob_shard(ctypes.byref(h), 0, 5000, 0x100, 0x100, 0x100, 0x100, None) == 1
+    assert b"whole" in lib.gh_last_error()
+    starts = (ctypes.c_int64 * 3)(0, 3000, 5000)
+    assert lib.grpo_logprob_merge(100, 5000, 2, starts, 0x100, 0x100, 0x100, 0x100, 0x100, 0x100, 0x100, 0x100,
+                                  None) == 1

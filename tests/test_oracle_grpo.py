@@ -190,3 +190,100 @@ def test_group_advantages_bernoulli_and_constant_groups():
     # mean 0.5, unbiased std sqrt(1/3): A = +-0.5/(sqrt(1/3)+1e-4)
     want = 0.5 / (math.sqrt(1.0 / 3.0) + 1e-4)
     np.testing.assert_allclose(A[4:], [-want, want, -want, want], atol=1e-12)
+
+
+# ---------------------------------------------------------------- two-sided cap, sequence-level ratio
+def test_two_sided_cap_worked_example():
+    # A = -1, r = 3, delta = 2: the capped unclipped term -2 is the min, so
+    # pg = 2 and the ratio gets no gradient (the cap binds); without the cap
+    # pg = 3 with gradient -A r = 3.  A = -1, r = 1.5 is below the cap:
+    # unchanged.  A = +1, r = 3 is clipped by eps either way (pg = -1.2).
+    r = np.array([3.0, 1.5, 3.0])
+    adv = np.array([-1.0, -1.0, 1.0])
+    logp = np.full(3, -2.0)
+    old = logp - np.log(r)
+    mask = np.ones(3, dtype=np.uint8)
+    seq = np.arange(3)
+    capped = oracle.grpo_loss(logp, old, None, mask, seq, adv, 3, 0.2, 0.2, 0.0, "fixed", 1.0, delta=2.0)
+    free = oracle.grpo_loss(logp, old, None, mask, seq, adv, 3, 0.2, 0.2, 0.0, "fixed", 1.0)
+    np.testing.assert_allclose(capped["per_seq_policy"], [2.0, 1.5, -1.2], atol=1e-12)
+    np.testing.assert_allclose(free["per_seq_policy"], [3.0, 1.5, -1.2], atol=1e-12)
+    np.testing.assert_allclose(capped["coef"], [0.0, 1.5, 0.0], atol=1e-12)
+    np.testing.assert_allclose(free["coef"], [3.0, 1.5, 0.0], atol=1e-12)
+
+
+def test_cap_above_every_ratio_changes_nothing():
+    logp, old, ref, mask, seq, adv, nseq = _grpo_case(21, spread=0.8)
+    rmax = float(np.exp(np.max((logp - old)[mask > 0])))
+    a = oracle.grpo_loss(logp, old, ref, mask, seq, adv, nseq, 0.2, 0.28, 0.05)
+    b = oracle.grpo_loss(logp, old, ref, mask, seq, adv, nseq, 0.2, 0.28, 0.05, delta=rmax * 1.01)
+    assert a["loss"] == b["loss"]
+    np.testing.assert_array_equal(a["coef"], b["coef"])
+
+
+def test_sequence_ratio_with_one_token_sequences_is_token_ratio():
+    rng = np.random.default_rng(22)
+    N = 30
+    logp = -rng.uniform(0.1, 4, N)
+    old = logp + rng.uniform(-0.6, 0.6, N)
+    ref = logp + rng.uniform(-0.2, 0.2, N)
+    adv = rng.standard_normal(N)
+    mask = np.ones(N, dtype=np.uint8)
+    seq = np.arange(N)
+    for red, norm in (("token_mean", 0.0), ("seq_mean", 0.0), ("fixed", 7.0)):
+        a = oracle.grpo_loss(logp, old, ref, mask, seq, adv, N, 0.2, 0.28, 0.1, red, norm, delta=1.6)
+        b = oracle.grpo_loss(logp, old, ref, mask, seq, adv, N, 0.2, 0.28, 0.1, red, norm, delta=1.6,
+                             ratio_level="sequence")
+        assert abs(a["loss"] - b["loss"]) < 1e-14
+        np.testing.assert_allclose(a["coef"], b["coef"], atol=1e-15)
+
+
+def test_sequence_ratio_with_constant_log_ratio_is_token_ratio():
+    # old = logp - c_s on every token of sequence s: every token ratio equals
+    # the sequence ratio, so both levels give the same loss and gradient
+    logp, old, ref, mask, seq, adv, nseq = _grpo_case(23, nseq=5, T=8)
+    c = np.random.default_rng(3).uniform(-0.5, 0.5, nseq)
+    old = logp - c[seq]
+    for red in ("token_mean", "seq_mean"):
+        a = oracle.grpo_loss(logp, old, ref, mask, seq, adv, nseq, 0.2, 0.28, 0.1, red)
+        b = oracle.grpo_loss(logp, old, ref, mask, seq, adv, nseq, 0.2, 0.28, 0.1, red, ratio_level="sequence")
+        assert abs(a["loss"] - b["loss"]) < 1e-14
+        np.testing.assert_allclose(a["coef"], b["coef"], atol=1e-14)
+
+
+def test_sequence_ratio_matches_token_weighted_gspo():
+    # beta = 0, fixed constant C: sum_s n_s pg_s / C, the GSPO loss with
+    # omega_s = n_s and divisor C (two independent oracle functions)
+    logp, old, ref, mask, seq, adv, nseq = _grpo_case(24, nseq=6, T=9, spread=0.4)
+    a = oracle.grpo_loss(logp, old, None, mask, seq, adv, nseq, 0.2, 0.28, 0.0, "fixed", 13.0,
+                         ratio_level="sequence")
+    g = oracle.gspo_loss(logp, old, mask, seq, nseq, adv, 0.2, 0.28, 13.0, token_weighted=True)
+    assert abs(a["loss"] - g["loss"]) < 1e-14
+    np.testing.assert_allclose(a["coef"], g["coef"], atol=1e-15)
+
+
+@pytest.mark.parametrize("ratio_level,delta", [("token", 1.15), ("sequence", 0.0), ("sequence", 1.1)])
+@pytest.mark.parametrize("reduction", ["token_mean", "seq_mean", "fixed"])
+def test_coef_is_derivative_with_cap_and_sequence_ratio(reduction, ratio_level, delta):
+    logp, old, ref, mask, seq, adv, nseq = _grpo_case(25, spread=0.5)
+    args = (old, ref, mask, seq, adv, nseq, 0.2, 0.28, 0.07, reduction, 37.0 if reduction == "fixed" else 0.0,
+            delta, ratio_level)
+    res = oracle.grpo_loss(logp, *args)
+    r = res["ratio"]
+    edges = [0.8, 1.28] + ([delta] if delta > 0 else [])
+    far = np.all([np.abs(r - e) > 1e-4 for e in edges], axis=0)
+    if ratio_level == "sequence":
+        far = np.array([far[seq == seq[i]].all() for i in range(len(logp))])
+    h = 1e-6
+    checked = 0
+    for i in range(len(logp)):
+        if not far[i]:
+            continue
+        lp = logp.copy()
+        lp[i] += h
+        up = oracle.grpo_loss(lp, *args)["loss"]
+        lp[i] -= 2 * h
+        dn = oracle.grpo_loss(lp, *args)["loss"]
+        assert abs((up - dn) / (2 * h) - res["coef"][i]) < 1e-7, (i, res["coef"][i])
+        checked += 1
+    assert checked > 20

@@ -46,7 +46,7 @@ def _call(lib, tensors, extra, num_seqs, noalloc):
     head = GhHead(N=N, D=D, V=V, dtype=0 if H.dtype == torch.bfloat16 else 1, row_tile=0, H=H.data_ptr(),
                   W=W.data_ptr(), targets=y.data_ptr(), mask=m.data_ptr())
     g = GhGrpo(old_logp=old.data_ptr(), ref_logp=ref.data_ptr(), adv=adv.data_ptr(), seq_id=seq.data_ptr(),
-               num_seqs=num_seqs, reduction=0, eps_low=0.2, eps_high=0.28, beta=0.04, reserved=0.0, norm=0.0)
+               num_seqs=num_seqs, reduction=0, eps_low=0.2, eps_high=0.28, beta=0.04, norm=0.0)
     out = {k: torch.full((N,), float("nan"), device="cuda") for k in ("logp", "lse", "coef")}
     out["loss3"] = torch.full((3,), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
