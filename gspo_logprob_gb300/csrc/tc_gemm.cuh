@@ -45,12 +45,14 @@ constexpr float LOG2E = 1.4426950408889634f;
 // accumulator; 2: 256 x 256 tiles whose two row blocks share every staged B
 // tile -- a third less shared-memory fill traffic per FLOP -- with a single
 // 2 x 256-column accumulator and twice the epilogue warps).
-template <int MT>
+// CG = epilogue warps per TMEM row (each takes 256 / CG of the tile's columns;
+// more warps drain a single-buffered accumulator sooner).
+template <int MT, int CG = 1>
 struct TcCfg {
   static constexpr int STAGE_BYTES = MT * TC_A_BYTES + TC_B_BYTES;
   static constexpr int STAGES = MT == 1 ? 4 : 3;
   static constexpr int NUM_ACC = MT == 1 ? 2 : 1;
-  static constexpr int EPI_WARPS = 4 * MT;
+  static constexpr int EPI_WARPS = 4 * MT * CG;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 };
@@ -81,12 +83,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int MT, bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(TcCfg<MT>::THREADS, 1)
+template <int MT, int CG, bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(TcCfg<MT, CG>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const TcSched sc, const int b_off_n, const int b_off_k, const typename Epi::Params ep,
                    int* status, const uint64_t timeout_ns) {
-  using C = TcCfg<MT>;
+  using C = TcCfg<MT, CG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -248,7 +250,10 @@ __global__ void __launch_bounds__(TcCfg<MT>::THREADS, 1)
   } else {
     // -------------------------------------------------- epilogue warps
     const int ew = warp - 2;
-    const int q = ew >> 2;      // which 128-row block of the tile
+    const int grp = ew >> 2;
+    const int q = grp / CG;     // which 128-row block of the tile
+    const int cg = grp % CG;    // which share of the columns
+    const int c_lo = cg * (TC_BN / 32 / CG), c_hi = c_lo + TC_BN / 32 / CG;
     const int sub = warp & 3;   // TMEM lane quarter this warp may access
     const int row = q * TC_BM + sub * 32 + lane;  // row within the CTA tile
     const uint32_t lane_addr = (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(q * TC_BN);
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(TcCfg<MT>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        epi.tile(ep, sc, tmem_base + lane_addr + static_cast<uint32_t>(acc * TC_BN), m_blk, n_blk, row);
+        epi.tile(ep, sc, tmem_base + lane_addr + static_cast<uint32_t>(acc * TC_BN), m_blk, n_blk, row, c_lo, c_hi);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -318,7 +323,8 @@ struct EpiFwdLse {
     y = valid ? __ldg(p.targets + grow) - p.col_offset : -1;  // local column of the target
   }
 
-  __device__ __forceinline__ void tile(const Params& p, const TcSched&, uint32_t taddr, int, int n_blk, int) {
+  // needs the whole row (online state across its columns): CG must be 1
+  __device__ __forceinline__ void tile(const Params& p, const TcSched&, uint32_t taddr, int, int n_blk, int, int, int) {
     float run_m = m, run_s = s;
     const int yy = y;
 #pragma unroll 1
@@ -391,7 +397,7 @@ struct EpiDlogits {
   __device__ __forceinline__ void end_task(const Params&, const TcSched&, int, int, int) {}
 
   __device__ __forceinline__ void tile(const Params& p, const TcSched& sc, uint32_t taddr, int m_blk, int n_blk,
-                                       int row) {
+                                       int row, int c_lo, int c_hi) {
     const int grow = m_blk * sc.m_step + row;
     const bool valid = grow < p.N;
     const float g = p.grad_out ? __ldg(p.grad_out) : 1.f;
@@ -399,7 +405,7 @@ struct EpiDlogits {
     const float lse2 = valid ? __ldg(p.lse + grow) * LOG2E : 0.f;
     const int yy = valid ? __ldg(p.targets + grow) - p.col_offset : -1;
 #pragma unroll 1
-    for (int c = 0; c < TC_BN / 32; ++c) {
+    for (int c = c_lo; c < c_hi; ++c) {
       float v[32];
       tmem_ld32(taddr + c * 32, v);
       const int lcol = n_blk * TC_BN + c * 32;  // column within the block
@@ -443,12 +449,12 @@ struct EpiStore {
   __device__ __forceinline__ void end_task(const Params&, const TcSched&, int, int, int) {}
 
   __device__ __forceinline__ void tile(const Params& p, const TcSched& sc, uint32_t taddr, int m_blk, int n_blk,
-                                       int row) {
+                                       int row, int c_lo, int c_hi) {
     const int lrow = m_blk * sc.m_step + row;
     const bool valid = lrow < p.M_valid;
     const size_t rbase = static_cast<size_t>(p.row_off + lrow) * p.ld;
 #pragma unroll 1
-    for (int c = 0; c < TC_BN / 32; ++c) {
+    for (int c = c_lo; c < c_hi; ++c) {
       float v[32];
       tmem_ld32(taddr + c * 32, v);
       const int col0 = n_blk * TC_BN + c * 32;

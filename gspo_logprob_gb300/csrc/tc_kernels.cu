@@ -36,6 +36,19 @@ int dw_mt() {
   static const int v = kind_mt("GH_DW_MT", 2);
   return v;
 }
+// epilogue warps per TMEM row for the 256-row tiles (1 or 2)
+int dlogits_cg() {
+  static const int v = kind_mt("GH_DLOGITS_CG", 1);
+  return v;
+}
+int dh_cg() {
+  static const int v = kind_mt("GH_DH_CG", 1);
+  return v;
+}
+int dw_cg() {
+  static const int v = kind_mt("GH_DW_CG", 1);
+  return v;
+}
 int kind_group_m(const char* name, int dflt) {
   const int v = env_int(name, dflt);
   return v > 0 ? v : dflt;
@@ -53,11 +66,11 @@ int dw_group_m() {
   return v;
 }
 
-template <int MT, bool A_MN, bool B_MN, class Epi>
+template <int MT, int CG, bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const TcSched& sc, int b_off_n, int b_off_k,
                       const typename Epi::Params& ep, int* status, cudaStream_t st) {
-  using C = TcCfg<MT>;
-  auto kern = tc_gemm_kernel<MT, A_MN, B_MN, Epi>;
+  using C = TcCfg<MT, CG>;
+  auto kern = tc_gemm_kernel<MT, CG, A_MN, B_MN, Epi>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -106,11 +119,11 @@ cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st) {
     const int m_step = a.row_tile;
     const int num_m = static_cast<int>(ceil_div(a.N, m_step));
     TcSched sc = make_sched(num_m, num_vt, TILES_PER_SPLIT, nkb, m_step, num_m);
-    return launch_tc<1, false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);
+    return launch_tc<1, 1, false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);
   }
   const int num_m = static_cast<int>(ceil_div(a.N, 2 * TC_BM));
   TcSched sc = make_sched(num_m, num_vt, TILES_PER_SPLIT, nkb, 2 * TC_BM, num_m);
-  return launch_tc<2, false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);
+  return launch_tc<2, 1, false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);
 }
 
 cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st) {
@@ -132,10 +145,11 @@ cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st) {
   const int nn = static_cast<int>(ceil_div(a.width, TC_BN));
   if (dlogits_mt() == 1) {
     TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, TC_BM)), nn, 1, nkb, TC_BM, dlogits_group_m());
-    return launch_tc<1, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
+    return launch_tc<1, 1, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
   }
   TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dlogits_group_m());
-  return launch_tc<2, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
+  if (dlogits_cg() == 2) return launch_tc<2, 2, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
+  return launch_tc<2, 1, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
 }
 
 cudaError_t launch_dh_tc(const TcDhArgs& a, cudaStream_t st) {
@@ -155,10 +169,11 @@ cudaError_t launch_dh_tc(const TcDhArgs& a, cudaStream_t st) {
   const int nn = static_cast<int>(ceil_div(a.D, TC_BN));
   if (dh_mt() == 1) {
     TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, TC_BM)), nn, 1, nkb, TC_BM, dh_group_m());
-    return launch_tc<1, false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
+    return launch_tc<1, 1, false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
   }
   TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dh_group_m());
-  return launch_tc<2, false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
+  if (dh_cg() == 2) return launch_tc<2, 2, false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
+  return launch_tc<2, 1, false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
 }
 
 cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st) {
@@ -180,10 +195,11 @@ cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st) {
   const int nn = static_cast<int>(ceil_div(a.D, TC_BN));
   if (dw_mt() == 1) {
     TcSched sc = make_sched(static_cast<int>(ceil_div(rows, TC_BM)), nn, 1, nkb, TC_BM, dw_group_m());
-    return launch_tc<1, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
+    return launch_tc<1, 1, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
   }
   TcSched sc = make_sched(static_cast<int>(ceil_div(rows, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dw_group_m());
-  return launch_tc<2, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
+  if (dw_cg() == 2) return launch_tc<2, 2, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
+  return launch_tc<2, 1, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
 }
 
 }  // namespace gh
