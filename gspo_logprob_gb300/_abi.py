@@ -22,7 +22,7 @@ GH_BF16, GH_FP32 = 0, 1
 GH_TOKEN_MEAN, GH_SEQ_MEAN, GH_FIXED = 0, 1, 2
 REDUCTIONS = {"token_mean": GH_TOKEN_MEAN, "seq_mean": GH_SEQ_MEAN, "fixed": GH_FIXED}
 RATIO_LEVELS = {"token": 0, "sequence": 1}
-NUM_KERNEL_KINDS = 14
+NUM_KERNEL_KINDS = 16
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # GH_NOALLOC_SCRATCH_BYTES
 
 
@@ -44,9 +44,15 @@ SIGNATURES = {
     "grpo_head_backward_workspace_size": (c_size_t, [POINTER(GhHead)]),
     "grpo_head_forward": (c_int32, [POINTER(GhHead), POINTER(GhGrpo), c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_size_t, c_void_p]),
-    "gspo_segment_loss": (c_int32, [c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_float,
-                                    c_float, c_double, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                    c_void_p]),
+    "gspo_segment_loss": (c_int32, [c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p,
+                                    c_float, c_float, c_float, c_double, c_int32, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, c_void_p, c_void_p]),
+    "gspo_segment_partials": (c_int32, [c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                        c_void_p, c_void_p, c_void_p, c_void_p]),
+    "gspo_segment_loss_from_partials": (c_int32, [c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
+                                                  c_void_p, c_void_p, c_void_p, c_float, c_float, c_float, c_double,
+                                                  c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                  c_void_p]),
     "grpo_head_backward": (c_int32, [POINTER(GhHead), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                      c_void_p, c_void_p, c_size_t, c_void_p]),
     "grpo_group_advantage": (c_int32, [c_void_p, c_int32, c_int32, c_float, c_void_p, c_void_p, c_void_p]),

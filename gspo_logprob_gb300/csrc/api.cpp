@@ -237,7 +237,7 @@ using namespace gh;
 
 extern "C" {
 
-int32_t gh_abi_version(void) { return 101; }
+int32_t gh_abi_version(void) { return 102; }
 
 const char* gh_status_string(gh_status s) {
   switch (s) {
@@ -422,26 +422,83 @@ gh_status grpo_loss_from_sequence_totals(int32_t num_seqs, const float* seq_poli
   return GH_OK;
 }
 
-gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp, const uint8_t* mask,
-                            const int32_t* seg_id, int32_t num_segments, const float* seg_adv, float eps_low,
-                            float eps_high, double divisor, int32_t token_weighted, float* loss, float* seg_ratio,
-                            float* coef, float* mean_logp, int32_t* status, void* stream) {
-  g_last_error.clear();
+static gh_status check_gspo_common(int64_t N, const float* logp, const uint8_t* mask, const int32_t* seg_id,
+                                   int32_t num_segments, int32_t* status) {
   if (N < 0 || N > (int64_t(1) << 30)) return fail(GH_ERR_INVALID_ARG, "N out of range");
-  if (!status || !loss || !seg_adv) return fail(GH_ERR_INVALID_ARG, "status/loss/seg_adv is NULL");
-  if (N > 0 && (!logp || !old_logp || !mask || !seg_id || !coef))
-    return fail(GH_ERR_INVALID_ARG, "logp/old_logp/mask/seg_id/coef is NULL");
+  if (!status) return fail(GH_ERR_INVALID_ARG, "status is NULL");
+  if (N > 0 && (!logp || !mask || !seg_id)) return fail(GH_ERR_INVALID_ARG, "logp/mask/seg_id is NULL");
   if (num_segments < 1 || num_segments > MAX_SEQS)
     return fail(GH_ERR_INVALID_ARG, "num_segments=%d out of [1, %d]", num_segments, MAX_SEQS);
+  return GH_OK;
+}
+
+static gh_status check_gspo_loss_args(const float* ref_logp, float beta, const float* seg_adv, float eps_low,
+                                      float eps_high, double divisor, float* loss, float* coef, int64_t N) {
+  if (!loss || !seg_adv) return fail(GH_ERR_INVALID_ARG, "loss/seg_adv is NULL");
+  if (N > 0 && !coef) return fail(GH_ERR_INVALID_ARG, "coef is NULL");
   if (!(divisor > 0.0) || !std::isfinite(divisor)) return fail(GH_ERR_INVALID_ARG, "divisor must be > 0");
   if (!(eps_low >= 0.f) || !(eps_high >= 0.f)) return fail(GH_ERR_INVALID_ARG, "eps must be >= 0");
+  if (!std::isfinite(beta) || (beta != 0.f && !ref_logp))
+    return fail(GH_ERR_INVALID_ARG, "beta must be finite, and ref_logp given when beta != 0");
+  return GH_OK;
+}
+
+gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp, const float* ref_logp,
+                            const uint8_t* mask, const int32_t* seg_id, int32_t num_segments, const float* seg_adv,
+                            float eps_low, float eps_high, float beta, double divisor, int32_t token_weighted,
+                            float* loss, float* seg_ratio, float* coef, float* mean_logp, int32_t* status,
+                            void* stream) {
+  g_last_error.clear();
+  gh_status s = check_gspo_common(N, logp, mask, seg_id, num_segments, status);
+  if (s != GH_OK) return s;
+  if (N > 0 && !old_logp) return fail(GH_ERR_INVALID_ARG, "old_logp is NULL");
+  s = check_gspo_loss_args(ref_logp, beta, seg_adv, eps_low, eps_high, divisor, loss, coef, N);
+  if (s != GH_OK) return s;
   if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = run(K_GSPO, st, [&] {
-    return launch_gspo(static_cast<int>(N), logp, old_logp, mask, seg_id, num_segments, seg_adv, eps_low, eps_high,
-                       divisor, token_weighted, loss, seg_ratio, coef, mean_logp, status, st);
-  });
+  GspoArgs g{static_cast<int>(N), logp, old_logp, beta != 0.f ? ref_logp : nullptr, mask, seg_id, num_segments,
+             seg_adv, eps_low, eps_high, beta, divisor, token_weighted, loss, seg_ratio, coef, mean_logp, status};
+  cudaError_t e = run(K_GSPO, st, [&] { return launch_gspo(g, st); });
   if (e != cudaSuccess) return cuda_fail(e, "GSPO launch");
+  return GH_OK;
+}
+
+gh_status gspo_segment_partials(int64_t N, const float* logp, const float* old_logp, const float* ref_logp,
+                                const uint8_t* mask, const int32_t* seg_id, int32_t num_segments, float* fsum,
+                                int32_t* cnt, int32_t* status, void* stream) {
+  g_last_error.clear();
+  gh_status s = check_gspo_common(N, logp, mask, seg_id, num_segments, status);
+  if (s != GH_OK) return s;
+  if (N > 0 && !old_logp) return fail(GH_ERR_INVALID_ARG, "old_logp is NULL");
+  if (!fsum || !cnt) return fail(GH_ERR_INVALID_ARG, "fsum/cnt is NULL");
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GspoArgs g{static_cast<int>(N), logp, old_logp, ref_logp, mask, seg_id, num_segments, nullptr, 0.f, 0.f, 0.f,
+             1.0, 0, nullptr, nullptr, nullptr, nullptr, status};
+  cudaError_t e = run(K_GSPO_PARTIALS, st, [&] { return launch_gspo_partials(g, fsum, cnt, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "GSPO partials launch");
+  return GH_OK;
+}
+
+gh_status gspo_segment_loss_from_partials(int64_t N, const float* logp, const float* ref_logp, const uint8_t* mask,
+                                          const int32_t* seg_id, int32_t num_segments, int32_t num_ranks,
+                                          const float* fsum_all, const int32_t* cnt_all, const float* seg_adv,
+                                          float eps_low, float eps_high, float beta, double divisor,
+                                          int32_t token_weighted, float* loss, float* seg_ratio, float* coef,
+                                          float* mean_logp, int32_t* status, void* stream) {
+  g_last_error.clear();
+  gh_status s = check_gspo_common(N, logp, mask, seg_id, num_segments, status);
+  if (s != GH_OK) return s;
+  s = check_gspo_loss_args(ref_logp, beta, seg_adv, eps_low, eps_high, divisor, loss, coef, N);
+  if (s != GH_OK) return s;
+  if (num_ranks < 1 || num_ranks > 4096) return fail(GH_ERR_INVALID_ARG, "num_ranks out of [1, 4096]");
+  if (!fsum_all || !cnt_all) return fail(GH_ERR_INVALID_ARG, "fsum_all/cnt_all is NULL");
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GspoArgs g{static_cast<int>(N), logp, nullptr, beta != 0.f ? ref_logp : nullptr, mask, seg_id, num_segments,
+             seg_adv, eps_low, eps_high, beta, divisor, token_weighted, loss, seg_ratio, coef, mean_logp, status};
+  cudaError_t e = run(K_GSPO_FINISH, st, [&] { return launch_gspo_finish(g, num_ranks, fsum_all, cnt_all, st); });
+  if (e != cudaSuccess) return cuda_fail(e, "GSPO finish launch");
   return GH_OK;
 }
 
@@ -560,7 +617,7 @@ const char* gh_kernel_kind_name(int32_t kind) {
   static const char* names[GH_NUM_KERNEL_KINDS] = {
       "fwd_logits_lse_tc", "merge_lse", "grpo_loss", "gspo_segment", "dlogits_tc", "dh_gemm_tc",
       "dw_gemm_tc", "group_advantage", "fwd_logits_lse_f32", "dlogits_f32", "gemm_f32", "timeout_probe",
-      "grpo_sequence_totals", "merge_lse_shards"};
+      "grpo_sequence_totals", "merge_lse_shards", "gspo_partials", "gspo_finish"};
   if (kind < 0 || kind >= GH_NUM_KERNEL_KINDS) return "";
   return names[kind];
 }

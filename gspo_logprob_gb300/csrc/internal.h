@@ -39,6 +39,8 @@ enum KernelKind {
   K_PROBE = 11,
   K_GRPO_TOTALS = 12,
   K_MERGE_SHARDS = 13,
+  K_GSPO_PARTIALS = 14,
+  K_GSPO_FINISH = 15,
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -165,10 +167,28 @@ cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_
                         float* loss3, int* status, cudaStream_t st);
 cudaError_t launch_grpo_totals(int num_seqs, const float* seq_policy, const float* seq_kl, const int32_t* seq_count,
                                int reduction, double norm, float beta, float* loss3, int* status, cudaStream_t st);
-cudaError_t launch_gspo(int N, const float* logp, const float* old_logp, const uint8_t* mask,
-                        const int32_t* seg_id, int num_segments, const float* seg_adv, float eps_low,
-                        float eps_high, double divisor, int token_weighted, float* loss, float* seg_ratio,
-                        float* coef, float* mean_logp, int* status, cudaStream_t st);
+struct GspoArgs {
+  int N;
+  const float* logp;
+  const float* old_logp;
+  const float* ref_logp;
+  const uint8_t* mask;
+  const int32_t* seg_id;
+  int num_segments;
+  const float* seg_adv;
+  float eps_low, eps_high, beta;
+  double divisor;
+  int token_weighted;
+  float* loss;
+  float* seg_ratio;
+  float* coef;
+  float* mean_logp;
+  int* status;
+};
+cudaError_t launch_gspo(const GspoArgs& g, cudaStream_t st);
+cudaError_t launch_gspo_partials(const GspoArgs& g, float* fsum, int32_t* cnt, cudaStream_t st);
+cudaError_t launch_gspo_finish(const GspoArgs& g, int R, const float* fsum_all, const int32_t* cnt_all,
+                               cudaStream_t st);
 cudaError_t launch_advantage(const float* rewards, int num_seqs, int group_size, float eps, float* adv,
                              cudaStream_t st);
 cudaError_t launch_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t st);

@@ -366,11 +366,12 @@ struct GspoP {
   int N;
   const float* logp;
   const float* old_logp;
+  const float* ref_logp;  // nullable (beta == 0)
   const uint8_t* mask;
   const int* seg_id;
   int num_segments;
   const float* seg_adv;
-  float eps_low, eps_high;
+  float eps_low, eps_high, beta;
   double divisor;
   int token_weighted;
   float* loss;
@@ -380,39 +381,32 @@ struct GspoP {
   int* status;
 };
 
-// one CTA of 1024 threads; dynamic shared memory: 2 * num_segments floats
-__global__ void __launch_bounds__(1024) gspo_kernel(GspoP p) {
-  extern __shared__ float sh[];
-  float* sL = sh;                     // omega_s l_s / divisor
-  float* sG = sh + p.num_segments;    // d loss / d logp for an active token of s
-  __shared__ float red_a[32], red_b[32];
-  __shared__ int s_nvalid;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nw = blockDim.x >> 5;
-  const float lo = 1.f - p.eps_low, hi = 1.f + p.eps_high;
-  const float inv_div = static_cast<float>(1.0 / p.divisor);
-
-  // phase 0: layout -- ids in [-1, S); ids >= 0 nondecreasing; -1 only as a tail, with mask 0
+// Layout check (ids in [-1, S); ids >= 0 nondecreasing; -1 only as a tail,
+// with mask 0) and the start of the -1 tail.  Block-wide; false on a bad
+// layout, after flagging it and zeroing coef.
+__device__ bool gspo_layout(const GspoP& p, int* s_nvalid) {
+  const int t = threadIdx.x;
   bool bad = false;
   for (int i = t; i < p.N; i += blockDim.x) {
-    const int s = p.seg_id[i];
-    if (s < -1 || s >= p.num_segments) bad = true;
-    if (s < 0 && p.mask[i]) bad = true;
+    const int sg = p.seg_id[i];
+    if (sg < -1 || sg >= p.num_segments) bad = true;
+    if (sg < 0 && p.mask[i]) bad = true;
     if (i > 0) {
       const int q = p.seg_id[i - 1];
-      if (q < 0 && s >= 0) bad = true;
-      if (q >= 0 && s >= 0 && q > s) bad = true;
+      if (q < 0 && sg >= 0) bad = true;
+      if (q >= 0 && sg >= 0 && q > sg) bad = true;
     }
   }
   if (__syncthreads_or(bad)) {
     if (t == 0) {
       atomicOr(p.status, GH_DEV_BAD_SEQ);
-      p.loss[0] = __int_as_float(0x7fc00000);
+      if (p.loss) p.loss[0] = __int_as_float(0x7fc00000);
     }
-    for (int i = t; i < p.N; i += blockDim.x) p.coef[i] = 0.f;
-    return;
+    if (p.coef)
+      for (int i = t; i < p.N; i += blockDim.x) p.coef[i] = 0.f;
+    return false;
   }
   if (t == 0) {
-    // first index of the -1 tail (predicate seg < 0 is monotone after the check)
     int lo_i = 0, hi_i = p.N;
     while (lo_i < hi_i) {
       const int mid = (lo_i + hi_i) >> 1;
@@ -421,78 +415,193 @@ __global__ void __launch_bounds__(1024) gspo_kernel(GspoP p) {
       else
         hi_i = mid;
     }
-    s_nvalid = lo_i;
+    *s_nvalid = lo_i;
   }
   __syncthreads();
-  const int nvalid = s_nvalid;
+  return true;
+}
 
-  // phase 1: warp per segment: S_s, n_s -> rho_s, l_s, per-token gradient
+// Per-segment partial sums of this call's tokens (warp per segment, lane-
+// strided in token order, then a xor butterfly): fS[s] = sum m (logp - old),
+// fK[s] = sum m kl, cnt[s] = active tokens; and *lps / *lpn = sum m logp and
+// sum m over all tokens (fixed shared-memory tree).
+__device__ void gspo_partials(const GspoP& p, int nvalid, float* fS, float* fK, int* cnt, float* lps, int* lpn,
+                              float* red_a, int* red_b) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nw = blockDim.x >> 5;
   bool nonfinite = false;
-  for (int s = warp; s < p.num_segments; s += nw) {
-    const int b = lower_bound_i(p.seg_id, 0, nvalid, s);
-    const int e = lower_bound_i(p.seg_id, b, nvalid, s + 1);
-    float acc = 0.f;
-    int cnt = 0;
+  for (int sg = warp; sg < p.num_segments; sg += nw) {
+    const int b = lower_bound_i(p.seg_id, 0, nvalid, sg);
+    const int e = lower_bound_i(p.seg_id, b, nvalid, sg + 1);
+    float acc = 0.f, kacc = 0.f;
+    int c = 0;
     for (int i = b + lane; i < e; i += 32) {
       if (!p.mask[i]) continue;
-      acc += p.logp[i] - p.old_logp[i];
-      cnt += 1;
+      const float lp = p.logp[i];
+      acc += lp - p.old_logp[i];
+      if (p.ref_logp) {
+        const float d = p.ref_logp[i] - lp;
+        kacc += expm1f(d) - d;
+      }
+      c += 1;
     }
     acc = wsum(acc);
-    cnt = wsum_i(cnt);
+    kacc = wsum(kacc);
+    c = wsum_i(c);
+    if (!isfinite(acc) || !isfinite(kacc)) nonfinite = true;
     if (lane == 0) {
-      float rho = 1.f, ell = 0.f, g = 0.f;
-      if (cnt > 0) {
-        const float A = p.seg_adv[s];
-        rho = expf(acc / static_cast<float>(cnt));
-        const float c = fminf(fmaxf(rho, lo), hi);
-        ell = -fminf(rho * A, c * A);
-        const bool act = A >= 0.f ? (rho <= hi) : (rho >= lo);
-        const float omega = p.token_weighted ? static_cast<float>(cnt) : 1.f;
-        ell = ell * omega * inv_div;
-        g = act ? (omega * inv_div) * (-A * rho) / static_cast<float>(cnt) : 0.f;
-        if (!isfinite(rho) || !isfinite(ell)) nonfinite = true;
-      }
-      sL[s] = ell;
-      sG[s] = g;
-      if (p.seg_ratio) p.seg_ratio[s] = rho;
+      fS[sg] = acc;
+      fK[sg] = kacc;
+      cnt[sg] = c;
     }
   }
   if (nonfinite) atomicOr(p.status, GH_DEV_NONFINITE);
-
-  // mean active logp: per-thread strided sums, then a fixed tree
-  float lps = 0.f;
-  int lpn = 0;
+  float a = 0.f;
+  int n = 0;
   for (int i = t; i < p.N; i += blockDim.x)
     if (p.mask[i]) {
-      lps += p.logp[i];
-      lpn += 1;
+      a += p.logp[i];
+      n += 1;
     }
-  lps = wsum(lps);
-  lpn = wsum_i(lpn);
+  a = wsum(a);
+  n = wsum_i(n);
   if (lane == 0) {
-    red_a[warp] = lps;
-    red_b[warp] = __int_as_float(lpn);
+    red_a[warp] = a;
+    red_b[warp] = n;
   }
   __syncthreads();
   if (warp == 0) {
-    float a = lane < nw ? red_a[lane] : 0.f;
-    int n = lane < nw ? __float_as_int(red_b[lane]) : 0;
-    a = wsum(a);
-    n = wsum_i(n);
+    float x = lane < nw ? red_a[lane] : 0.f;
+    int y = lane < nw ? red_b[lane] : 0;
+    x = wsum(x);
+    y = wsum_i(y);
+    if (lane == 0) {
+      *lps = x;
+      *lpn = y;
+    }
+  }
+  __syncthreads();
+}
+
+// Loss from the partials of R contiguous pieces of the batch (R = 1 for one
+// call; sequence-parallel ranks otherwise), summed over pieces in order:
+// rho_s = exp(S_s / n_s), l_s = -min(rho A, clip(rho) A), K_s = mean k3 KL,
+// loss = sum_s (omega_s / divisor)(l_s + beta K_s).  Leaves per segment
+// sL = loss term, sG = policy gradient per active token, sB = KL gradient
+// scale per active token (these may alias fS, fK, cnt when R = 1: each
+// segment is read and then written by the same thread).  Writes loss,
+// seg_ratio and mean_logp.
+__device__ void gspo_finish(const GspoP& p, int R, int fstride, int cstride, const float* fS, const float* fK,
+                            const int* cnt, const float* lps, const int* lpn, float* sL, float* sG, float* sB) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const float lo = 1.f - p.eps_low, hi = 1.f + p.eps_high;
+  const float inv_div = static_cast<float>(1.0 / p.divisor);
+  bool nonfinite = false;
+  for (int sg = t; sg < p.num_segments; sg += blockDim.x) {
+    float S = 0.f, K = 0.f;
+    int n = 0;
+    for (int r = 0; r < R; ++r) {
+      S += fS[r * fstride + sg];
+      K += fK[r * fstride + sg];
+      n += cnt[r * cstride + sg];
+    }
+    float rho = 1.f, ell = 0.f, g = 0.f, kb = 0.f;
+    if (n > 0) {
+      const float A = p.seg_adv[sg];
+      const float nf = static_cast<float>(n);
+      rho = expf(S / nf);
+      const float c = fminf(fmaxf(rho, lo), hi);
+      const float u = rho * A, v = c * A;
+      const float pol = -fminf(u, v);
+      const bool act = (u <= v) ? true : (rho >= lo && rho <= hi);
+      const float omega = p.token_weighted ? nf : 1.f;
+      ell = omega * inv_div * (pol + p.beta * (K / nf));
+      g = act ? (omega * inv_div) * (-A * rho) / nf : 0.f;
+      kb = (omega * inv_div) * p.beta / nf;
+      if (!isfinite(rho) || !isfinite(ell)) nonfinite = true;
+    }
+    sL[sg] = ell;
+    sG[sg] = g;
+    sB[sg] = kb;
+    if (p.seg_ratio) p.seg_ratio[sg] = rho;
+  }
+  if (nonfinite) atomicOr(p.status, GH_DEV_NONFINITE);
+  __syncthreads();
+  if (warp == 0) {
     float L = 0.f;
-    for (int s = lane; s < p.num_segments; s += 32) L += sL[s];
+    for (int sg = lane; sg < p.num_segments; sg += 32) L += sL[sg];
     L = wsum(L);
     if (lane == 0) {
       p.loss[0] = L;
-      if (p.mean_logp) p.mean_logp[0] = n > 0 ? a / static_cast<float>(n) : 0.f;
+      if (p.mean_logp) {
+        float a = 0.f;
+        int n = 0;
+        for (int r = 0; r < R; ++r) {
+          a += lps[r * fstride];
+          n += lpn[r * cstride];
+        }
+        p.mean_logp[0] = n > 0 ? a / static_cast<float>(n) : 0.f;
+      }
     }
   }
-  // phase 2: coef
-  for (int i = t; i < p.N; i += blockDim.x) {
-    const int s = p.seg_id[i];
-    p.coef[i] = (s >= 0 && p.mask[i]) ? sG[s] : 0.f;
+}
+
+// coef_i = m_i (sG[s] + sB[s] (1 - exp(ref_i - logp_i))) for this call's tokens
+__device__ void gspo_coef(const GspoP& p, const float* sG, const float* sB) {
+  for (int i = threadIdx.x; i < p.N; i += blockDim.x) {
+    const int sg = p.seg_id[i];
+    float c = 0.f;
+    if (sg >= 0 && p.mask[i]) {
+      c = sG[sg];
+      if (p.ref_logp) c -= sB[sg] * expm1f(p.ref_logp[i] - p.logp[i]);
+    }
+    p.coef[i] = c;
   }
+}
+
+// one call over the whole batch: one CTA of 1024 threads; dynamic shared
+// memory 3 * num_segments words (partials, reused for the per-segment results)
+__global__ void __launch_bounds__(1024) gspo_kernel(GspoP p) {
+  extern __shared__ float sh[];
+  float* fS = sh;
+  float* fK = sh + p.num_segments;
+  int* cnt = reinterpret_cast<int*>(sh + 2 * p.num_segments);
+  __shared__ float red_a[32];
+  __shared__ int red_b[32];
+  __shared__ int s_nvalid;
+  __shared__ float s_lps;
+  __shared__ int s_lpn;
+  if (!gspo_layout(p, &s_nvalid)) return;
+  gspo_partials(p, s_nvalid, fS, fK, cnt, &s_lps, &s_lpn, red_a, red_b);
+  gspo_finish(p, 1, 0, 0, fS, fK, cnt, &s_lps, &s_lpn, fS, fK, reinterpret_cast<float*>(cnt));
+  __syncthreads();
+  gspo_coef(p, fS + p.num_segments, reinterpret_cast<float*>(cnt));
+}
+
+// sequence-parallel step 1: this rank's partials to global memory
+// fsum [2S + 1] = (S_s..., K_s..., sum m logp), cnt [S + 1] = (n_s..., sum m)
+__global__ void __launch_bounds__(1024) gspo_partials_kernel(GspoP p, float* fsum, int* cnt) {
+  __shared__ float red_a[32];
+  __shared__ int red_b[32];
+  __shared__ int s_nvalid;
+  if (!gspo_layout(p, &s_nvalid)) return;
+  const int S = p.num_segments;
+  gspo_partials(p, s_nvalid, fsum, fsum + S, cnt, fsum + 2 * S, cnt + S, red_a, red_b);
+}
+
+// sequence-parallel step 2: loss from R ranks' gathered partials, coef for
+// this rank's tokens; dynamic shared memory 3 * num_segments words
+__global__ void __launch_bounds__(1024) gspo_finish_kernel(GspoP p, int R, const float* fsum_all,
+                                                           const int* cnt_all) {
+  extern __shared__ float sh[];
+  float* sL = sh;
+  float* sG = sh + p.num_segments;
+  float* sB = sh + 2 * p.num_segments;
+  __shared__ int s_nvalid;
+  if (!gspo_layout(p, &s_nvalid)) return;
+  const int S = p.num_segments;
+  gspo_finish(p, R, 2 * S + 1, S + 1, fsum_all, fsum_all + S, cnt_all, fsum_all + 2 * S, cnt_all + S, sL, sG, sB);
+  __syncthreads();
+  gspo_coef(p, sG, sB);
 }
 
 // ---------------------------------------------------------------- advantages
@@ -598,35 +707,57 @@ cudaError_t launch_grpo_totals(int num_seqs, const float* seq_policy, const floa
   return cudaGetLastError();
 }
 
-cudaError_t launch_gspo(int N, const float* logp, const float* old_logp, const uint8_t* mask, const int32_t* seg_id,
-                        int num_segments, const float* seg_adv, float eps_low, float eps_high, double divisor,
-                        int token_weighted, float* loss, float* seg_ratio, float* coef, float* mean_logp,
-                        int* status, cudaStream_t st) {
+static GspoP gspo_params(const GspoArgs& g) {
   GspoP p;
-  p.N = N;
-  p.logp = logp;
-  p.old_logp = old_logp;
-  p.mask = mask;
-  p.seg_id = seg_id;
-  p.num_segments = num_segments;
-  p.seg_adv = seg_adv;
-  p.eps_low = eps_low;
-  p.eps_high = eps_high;
-  p.divisor = divisor;
-  p.token_weighted = token_weighted;
-  p.loss = loss;
-  p.seg_ratio = seg_ratio;
-  p.coef = coef;
-  p.mean_logp = mean_logp;
-  p.status = status;
+  p.N = g.N;
+  p.logp = g.logp;
+  p.old_logp = g.old_logp;
+  p.ref_logp = g.ref_logp;
+  p.mask = g.mask;
+  p.seg_id = g.seg_id;
+  p.num_segments = g.num_segments;
+  p.seg_adv = g.seg_adv;
+  p.eps_low = g.eps_low;
+  p.eps_high = g.eps_high;
+  p.beta = g.beta;
+  p.divisor = g.divisor;
+  p.token_weighted = g.token_weighted;
+  p.loss = g.loss;
+  p.seg_ratio = g.seg_ratio;
+  p.coef = g.coef;
+  p.mean_logp = g.mean_logp;
+  p.status = g.status;
+  return p;
+}
+
+cudaError_t launch_gspo(const GspoArgs& g, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(gspo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         2 * MAX_SEQS * static_cast<int>(sizeof(float)));
+                                         3 * MAX_SEQS * static_cast<int>(sizeof(float)));
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  gspo_kernel<<<1, 1024, static_cast<size_t>(2) * num_segments * sizeof(float), st>>>(p);
+  gspo_kernel<<<1, 1024, static_cast<size_t>(3) * g.num_segments * sizeof(float), st>>>(gspo_params(g));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gspo_partials(const GspoArgs& g, float* fsum, int32_t* cnt, cudaStream_t st) {
+  gspo_partials_kernel<<<1, 1024, 0, st>>>(gspo_params(g), fsum, cnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gspo_finish(const GspoArgs& g, int R, const float* fsum_all, const int32_t* cnt_all,
+                               cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gspo_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         3 * MAX_SEQS * static_cast<int>(sizeof(float)));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  gspo_finish_kernel<<<1, 1024, static_cast<size_t>(3) * g.num_segments * sizeof(float), st>>>(gspo_params(g), R,
+                                                                                               fsum_all, cnt_all);
   return cudaGetLastError();
 }
 

@@ -231,13 +231,16 @@ def grpo_loss_from_sequence_totals(seq_policy, seq_kl, seq_count, *, reduction: 
 
 
 def gspo_segment_loss(logp, old_logp, mask, seg_id, num_segments: int, seg_adv, *, eps_low: float,
-                      eps_high: float, divisor: float, token_weighted: bool = False,
-                      status: Optional[torch.Tensor] = None):
-    """GSPO sequence-level loss over packed documents; returns loss [1],
-    seg_ratio [S], coef [N], mean_logp [1] and status."""
+                      eps_high: float, divisor: float, token_weighted: bool = False, ref_logp=None,
+                      beta: float = 0.0, status: Optional[torch.Tensor] = None):
+    """GSPO sequence-level loss over packed documents (optionally with a
+    per-segment mean k3 KL weighted by beta); returns loss [1], seg_ratio [S],
+    coef [N], mean_logp [1] and status."""
     N = logp.numel()
     _need(logp, "logp", _F32, (N,))
     _need(old_logp, "old_logp", _F32, (N,))
+    if ref_logp is not None:
+        _need(ref_logp, "ref_logp", _F32, (N,))
     _need(mask, "mask", torch.uint8, (N,))
     _need(seg_id, "seg_id", torch.int32, (N,))
     _need(seg_adv, "seg_adv", _F32, (num_segments,))
@@ -247,10 +250,59 @@ def gspo_segment_loss(logp, old_logp, mask, seg_id, num_segments: int, seg_adv, 
     coef = torch.empty(N, dtype=_F32, device=dev)
     mean_logp = torch.empty(1, dtype=_F32, device=dev)
     st = new_status(dev) if status is None else status
-    code = _lib().gspo_segment_loss(N, _ptr(logp), _ptr(old_logp), _ptr(mask), _ptr(seg_id), num_segments,
-                                    _ptr(seg_adv), eps_low, eps_high, float(divisor), 1 if token_weighted else 0,
-                                    _ptr(loss), _ptr(ratio), _ptr(coef), _ptr(mean_logp), _ptr(st), _stream(dev))
+    code = _lib().gspo_segment_loss(N, _ptr(logp), _ptr(old_logp), _ptr(ref_logp), _ptr(mask), _ptr(seg_id),
+                                    num_segments, _ptr(seg_adv), eps_low, eps_high, float(beta), float(divisor),
+                                    1 if token_weighted else 0, _ptr(loss), _ptr(ratio), _ptr(coef), _ptr(mean_logp),
+                                    _ptr(st), _stream(dev))
     _abi.check(code, "gspo_segment_loss")
+    return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, status=st)
+
+
+def gspo_segment_partials(logp, old_logp, mask, seg_id, num_segments: int, *, ref_logp=None,
+                          status: Optional[torch.Tensor] = None):
+    """One sequence-parallel rank's GSPO partials: fsum [2S + 1], cnt [S + 1]."""
+    N = logp.numel()
+    _need(logp, "logp", _F32, (N,))
+    _need(old_logp, "old_logp", _F32, (N,))
+    _need(mask, "mask", torch.uint8, (N,))
+    _need(seg_id, "seg_id", torch.int32, (N,))
+    dev = logp.device
+    fsum = torch.empty(2 * num_segments + 1, dtype=_F32, device=dev)
+    cnt = torch.empty(num_segments + 1, dtype=torch.int32, device=dev)
+    st = new_status(dev) if status is None else status
+    code = _lib().gspo_segment_partials(N, _ptr(logp), _ptr(old_logp), _ptr(ref_logp), _ptr(mask), _ptr(seg_id),
+                                        num_segments, _ptr(fsum), _ptr(cnt), _ptr(st), _stream(dev))
+    _abi.check(code, "gspo_segment_partials")
+    return dict(fsum=fsum, cnt=cnt, status=st)
+
+
+def gspo_segment_loss_from_partials(logp, mask, seg_id, num_segments: int, fsum_all, cnt_all, seg_adv, *,
+                                    eps_low: float, eps_high: float, divisor: float, token_weighted: bool = False,
+                                    ref_logp=None, beta: float = 0.0, status: Optional[torch.Tensor] = None):
+    """GSPO loss from the ranks' gathered partials ([R, 2S + 1], [R, S + 1]);
+    coef for this rank's tokens."""
+    N = logp.numel()
+    R = fsum_all.shape[0]
+    _need(logp, "logp", _F32, (N,))
+    _need(mask, "mask", torch.uint8, (N,))
+    _need(seg_id, "seg_id", torch.int32, (N,))
+    _need(fsum_all, "fsum_all", _F32, (R, 2 * num_segments + 1))
+    _need(cnt_all, "cnt_all", torch.int32, (R, num_segments + 1))
+    _need(seg_adv, "seg_adv", _F32, (num_segments,))
+    if ref_logp is not None:
+        _need(ref_logp, "ref_logp", _F32, (N,))
+    dev = logp.device
+    loss = torch.empty(1, dtype=_F32, device=dev)
+    ratio = torch.empty(num_segments, dtype=_F32, device=dev)
+    coef = torch.empty(N, dtype=_F32, device=dev)
+    mean_logp = torch.empty(1, dtype=_F32, device=dev)
+    st = new_status(dev) if status is None else status
+    code = _lib().gspo_segment_loss_from_partials(N, _ptr(logp), _ptr(ref_logp), _ptr(mask), _ptr(seg_id),
+                                                  num_segments, R, _ptr(fsum_all), _ptr(cnt_all), _ptr(seg_adv),
+                                                  eps_low, eps_high, float(beta), float(divisor),
+                                                  1 if token_weighted else 0, _ptr(loss), _ptr(ratio), _ptr(coef),
+                                                  _ptr(mean_logp), _ptr(st), _stream(dev))
+    _abi.check(code, "gspo_segment_loss_from_partials")
     return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, status=st)
 
 

@@ -201,19 +201,48 @@ gh_status grpo_loss_from_sequence_totals(int32_t num_seqs, const float* seq_poli
  * GSPO sequence-level loss over packed documents (Fast-LLM PR #554, What):
  *   S_s = sum_{i in s} m_i (logp_i - old_i), n_s = sum_{i in s} m_i,
  *   rho_s = exp(S_s / n_s), l_s = -min(rho_s A_s, clip(rho_s) A_s),
- *   loss = sum_s omega_s l_s / divisor, omega_s = 1 (or n_s if token_weighted),
- *   coef_i = (omega_s / divisor) (-A_s rho_s act_s) m_i / n_s.
+ *   K_s = (1/n_s) sum_{i in s} m_i (exp(d_i) - d_i - 1), d = ref - logp,
+ *   loss = sum_s omega_s (l_s + beta K_s) / divisor, omega_s = 1 (or n_s if
+ *   token_weighted),
+ *   coef_i = (omega_s / divisor)(-A_s rho_s act_s + beta (1 - exp(d_i))) m_i / n_s.
  * seg_id [N]: document of each token; ids >= 0 are nondecreasing and -1 marks
  * an unused tail (whose mask must be 0).  Segments with n_s = 0 contribute 0
- * and report seg_ratio 1.  Outputs: loss [1], seg_ratio [num_segments],
- * coef [N], mean_logp [1] (the new_logprobs metric: mean active logp); any of
- * seg_ratio / mean_logp may be NULL.  No scratch memory is needed.
+ * and report seg_ratio 1.  ref_logp may be NULL when beta == 0.  Outputs:
+ * loss [1], seg_ratio [num_segments], coef [N], mean_logp [1] (the
+ * new_logprobs metric: mean active logp); seg_ratio / mean_logp may be NULL.
+ * No scratch memory is needed.
  */
-gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp, const uint8_t* mask,
-                            const int32_t* seg_id, int32_t num_segments, const float* seg_adv,
-                            float eps_low, float eps_high, double divisor, int32_t token_weighted,
-                            float* loss, float* seg_ratio, float* coef, float* mean_logp,
-                            int32_t* status, void* stream);
+gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp, const float* ref_logp,
+                            const uint8_t* mask, const int32_t* seg_id, int32_t num_segments, const float* seg_adv,
+                            float eps_low, float eps_high, float beta, double divisor, int32_t token_weighted,
+                            float* loss, float* seg_ratio, float* coef, float* mean_logp, int32_t* status,
+                            void* stream);
+
+/*
+ * GSPO under sequence parallelism (Fast-LLM PR #554, What / Correctness: the
+ * segment sums are reduced across the sequence-data-parallel ranks between
+ * the pre- and post-aggregation blocks; a document may span ranks).  Each
+ * rank holds a contiguous piece of the packed token sequence (same seg_id
+ * layout rule within its piece) and calls gspo_segment_partials, which writes
+ *   fsum [2 * num_segments + 1] = (S_s partial..., KL partial..., sum m logp),
+ *   cnt  [num_segments + 1]     = (n_s partial..., sum m);
+ * ref_logp NULL skips the KL partials.  The ranks gather fsum and cnt in rank
+ * order ([num_ranks, 2S + 1] and [num_ranks, S + 1]) and each calls
+ * gspo_segment_loss_from_partials for its own tokens: the partials are summed
+ * over ranks in rank order (no float all-reduce, so the result does not depend
+ * on the collective's topology), then loss, seg_ratio, mean_logp and this
+ * rank's coef follow as in gspo_segment_loss.  With one rank the result is
+ * bitwise gspo_segment_loss's.
+ */
+gh_status gspo_segment_partials(int64_t N, const float* logp, const float* old_logp, const float* ref_logp,
+                                const uint8_t* mask, const int32_t* seg_id, int32_t num_segments, float* fsum,
+                                int32_t* cnt, int32_t* status, void* stream);
+gh_status gspo_segment_loss_from_partials(int64_t N, const float* logp, const float* ref_logp, const uint8_t* mask,
+                                          const int32_t* seg_id, int32_t num_segments, int32_t num_ranks,
+                                          const float* fsum_all, const int32_t* cnt_all, const float* seg_adv,
+                                          float eps_low, float eps_high, float beta, double divisor,
+                                          int32_t token_weighted, float* loss, float* seg_ratio, float* coef,
+                                          float* mean_logp, int32_t* status, void* stream);
 
 /*
  * Backward of the head given each row's LSE and coef (from grpo_head_forward
@@ -277,9 +306,10 @@ int32_t gh_abi_version(void);
  * the recorded events).  gh_launch_count counts all launches since load.
  * Kinds: 0 fwd logits+LSE, 1 merge, 2 GRPO loss, 3 GSPO loss, 4 dlogits,
  * 5 dH GEMM, 6 dW GEMM, 7 advantage, 8 fp32 forward, 9 fp32 dlogits,
- * 10 fp32 GEMM, 11 timeout probe, 12 GRPO loss from sequence totals, 13 shard merge.
+ * 10 fp32 GEMM, 11 timeout probe, 12 GRPO loss from sequence totals, 13 shard merge,
+ * 14 GSPO partials, 15 GSPO loss from partials.
  */
-#define GH_NUM_KERNEL_KINDS 14
+#define GH_NUM_KERNEL_KINDS 16
 void gh_profile_enable(int32_t on);
 void gh_profile_reset(void);
 gh_status gh_profile_read(int32_t kind, int64_t* launches, double* total_ms);

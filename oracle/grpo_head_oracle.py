@@ -27,8 +27,10 @@ Pins (tests/test_oracle_*.py):
       with and without the two-sided cap), the cap's worked example, a cap
       above every ratio changes nothing, one-token sequences and constant
       per-sequence log-ratios reduce the sequence level to the token level
-  gspo_loss : length-1 segments reduce to token PPO-clip, one segment closed
-      form, np.bincount counts, finite differences w.r.t. logp
+  gspo_loss : length-1 segments reduce to token PPO-clip (with the KL term:
+      to the token-level GRPO loss with the same fixed normaliser), one
+      segment closed form, np.bincount counts, finite differences w.r.t. logp
+      with and without the KL term
   dlogits / head_backward : finite differences of the loss w.r.t. H and W,
       row sums of dlogits and column sums of dW vanish
 No function is "parity unpinned".
@@ -313,12 +315,15 @@ def grpo_loss(logp, old, ref, mask, seq_id, adv, num_seqs: int, eps_low: float,
 # grad_output applied outside)
 # --------------------------------------------------------------------------
 def gspo_loss(logp, old, mask, seg_id, num_segments: int, seg_adv, eps_low: float,
-              eps_high: float, divisor: float, token_weighted: bool = False):
+              eps_high: float, divisor: float, token_weighted: bool = False, ref=None, beta: float = 0.0):
     """S_s = sum_{i in s} m_i (logp_i - old_i) and n_s = sum m_i (explicit
     loop: the index_add_ of the seam); rho_s = exp(S_s / n_s);
     l_s = -min(rho_s A_s, clip(rho_s, 1-eps_low, 1+eps_high) A_s);
-    loss = sum_s omega_s l_s / divisor with omega_s = 1 (or n_s when
-    token_weighted); coef_i = (omega_s / divisor) (-A_s rho_s act_s) m_i / n_s;
+    with a reference policy, K_s = (1/n_s) sum_{i in s} m_i kl_i (k3, the
+    segment mean, matching the sequence-level ratio);
+    loss = sum_s omega_s (l_s + beta K_s) / divisor with omega_s = 1 (or n_s
+    when token_weighted); coef_i = d loss / d logp_i =
+    (omega_s / divisor) (-A_s rho_s act_s + beta (1 - e^{d_i})) m_i / n_s;
     segments with n_s = 0 contribute 0 and report rho = 1; tokens with
     seg_id = -1 belong to no segment; new_logprobs = mean active logp."""
     logp = np.asarray(logp, dtype=np.float64)
@@ -326,7 +331,10 @@ def gspo_loss(logp, old, mask, seg_id, num_segments: int, seg_adv, eps_low: floa
     N = logp.shape[0]
     if not divisor > 0:
         raise OracleError("divisor must be positive")
+    use_kl = ref is not None and beta != 0.0
+    rf = np.asarray(ref, dtype=np.float64) if use_kl else None
     S = np.zeros(num_segments)
+    K = np.zeros(num_segments)
     n = np.zeros(num_segments, dtype=np.int64)
     lp_sum = 0.0
     act_tokens = 0
@@ -335,34 +343,43 @@ def gspo_loss(logp, old, mask, seg_id, num_segments: int, seg_adv, eps_low: floa
         if mask[i] and s >= 0:
             S[s] += logp[i] - old[i]
             n[s] += 1
+            if use_kl:
+                d = rf[i] - logp[i]
+                K[s] += math.exp(d) - d - 1.0
         if mask[i]:
             lp_sum += logp[i]
             act_tokens += 1
     A = np.asarray(seg_adv, dtype=np.float64)
     rho = np.ones(num_segments)
     ell = np.zeros(num_segments)
-    g = np.zeros(num_segments)                           # d loss / d S_s * n_s
+    g = np.zeros(num_segments)                           # policy part of d loss / d logp, per active token
+    kb = np.zeros(num_segments)                          # KL part scale, per active token
     loss = 0.0
+    abs_terms = 0.0
     for s in range(num_segments):
         if n[s] == 0:
             continue
         rho[s] = math.exp(S[s] / n[s])
         c = min(max(rho[s], 1.0 - eps_low), 1.0 + eps_high)
-        ell[s] = -min(rho[s] * A[s], c * A[s])
-        act = (rho[s] <= 1.0 + eps_high) if A[s] >= 0 else (rho[s] >= 1.0 - eps_low)
+        u, v = rho[s] * A[s], c * A[s]
+        ell[s] = -min(u, v)
+        act = True if u <= v else (1.0 - eps_low <= rho[s] <= 1.0 + eps_high)
         omega = float(n[s]) if token_weighted else 1.0
-        loss += omega * ell[s] / divisor
-        g[s] = (omega / divisor) * (-A[s] * rho[s] * (1.0 if act else 0.0))
+        term = ell[s] + (beta * K[s] / n[s] if use_kl else 0.0)
+        loss += omega * term / divisor
+        abs_terms += abs(omega * term / divisor)
+        g[s] = (omega / divisor) * (-A[s] * rho[s] * (1.0 if act else 0.0)) / n[s]
+        kb[s] = (omega / divisor) * beta / n[s]
     coef = np.zeros(N)
     for i in range(N):
         s = int(seg_id[i])
         if mask[i] and s >= 0:
-            coef[i] = g[s] / n[s]
+            coef[i] = g[s]
+            if use_kl:
+                coef[i] += kb[s] * (1.0 - math.exp(rf[i] - logp[i]))
     mean_logp = lp_sum / act_tokens if act_tokens > 0 else 0.0
-    omega_all = n.astype(np.float64) if token_weighted else np.ones(num_segments)
-    abs_terms = float(np.sum(np.abs(omega_all * ell)) / divisor)
     return dict(loss=loss, seg_ratio=rho, seg_loss=ell, coef=coef, counts=n,
-                seg_sum=S, mean_logp=mean_logp, abs_terms=abs_terms)
+                seg_sum=S, seg_kl=K, mean_logp=mean_logp, abs_terms=abs_terms)
 
 
 # --------------------------------------------------------------------------

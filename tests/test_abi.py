@@ -60,7 +60,7 @@ def test_struct_layout_matches_c(lib, tmp_path):
 
 
 def test_host_only_calls(lib):
-    assert lib.gh_abi_version() == 101
+    assert lib.gh_abi_version() == 102
     assert lib.gh_status_string(0) == b"GH_OK"
     assert lib.gh_status_string(3) == b"GH_ERR_WORKSPACE"
     assert lib.gh_kernel_kind_name(0) == b"fwd_logits_lse_tc"
@@ -127,12 +127,15 @@ def test_no_gpu_fails_loudly(lib):
 
 
 def test_gspo_and_advantage_validation(lib):
-    st = lib.gspo_segment_loss(10, 0x100, 0x100, 0x100, 0x100, 0, 0x100, 0.2, 0.2, 1.0, 0, 0x100, None, 0x100,
-                               None, 0x100, None)
+    st = lib.gspo_segment_loss(10, 0x100, 0x100, None, 0x100, 0x100, 0, 0x100, 0.2, 0.2, 0.0, 1.0, 0, 0x100, None,
+                               0x100, None, 0x100, None)
     assert st == 1 and b"num_segments" in lib.gh_last_error()
-    st = lib.gspo_segment_loss(10, 0x100, 0x100, 0x100, 0x100, 4, 0x100, 0.2, 0.2, 0.0, 0, 0x100, None, 0x100,
-                               None, 0x100, None)
+    st = lib.gspo_segment_loss(10, 0x100, 0x100, None, 0x100, 0x100, 4, 0x100, 0.2, 0.2, 0.0, 0.0, 0, 0x100, None,
+                               0x100, None, 0x100, None)
     assert st == 1 and b"divisor" in lib.gh_last_error()
+    st = lib.gspo_segment_loss(10, 0x100, 0x100, None, 0x100, 0x100, 4, 0x100, 0.2, 0.2, 0.1, 1.0, 0, 0x100, None,
+                               0x100, None, 0x100, None)
+    assert st == 1 and b"ref_logp" in lib.gh_last_error()
     st = lib.grpo_group_advantage(0x100, 10, 4, 1e-4, 0x100, 0x100, None)
     assert st == 1 and b"multiple" in lib.gh_last_error()
 

@@ -126,3 +126,79 @@ def test_gspo_layout_errors(gpu_lib):
     mask2[5] = 0
     r = g.gspo_segment_loss(logp, logp, mask2, bad, 8, A, eps_low=0.2, eps_high=0.2, divisor=8.0)
     assert int(r["status"].item()) & 16
+
+
+def _gspo_inputs(masked_frac=0.1, seed=7):
+    cfg = CONFIGS[3]
+    w = make_workload(cfg, masked_frac=masked_frac, with_weight=False, old_noise=0.01)
+    rng = np.random.default_rng(seed)
+    N = cfg.N
+    logp = (-rng.uniform(0.05, 6.0, N)).astype(np.float32)
+    old = (logp.astype(np.float64) + w["u_old"]).astype(np.float32)
+    ref = (logp.astype(np.float64) + w["u_ref"]).astype(np.float32)
+    return cfg, w, logp, old, ref, _seg_adv(w)
+
+
+@pytest.mark.parametrize("token_weighted", [False, True])
+def test_gspo_kernel_with_kl_vs_oracle(gpu_lib, token_weighted):
+    import gspo_logprob_gb300 as g
+    cfg, w, logp, old, ref, A = _gspo_inputs()
+    S = cfg.num_docs
+    beta = 0.05
+    res = g.gspo_segment_loss(dev_tensor(logp), dev_tensor(old), dev_tensor(w["mask"]), dev_tensor(w["seq_id"]), S,
+                              dev_tensor(A), eps_low=0.2, eps_high=0.28, divisor=float(S),
+                              token_weighted=token_weighted, ref_logp=dev_tensor(ref), beta=beta)
+    o = oracle.gspo_loss(logp.astype(np.float64), old.astype(np.float64), w["mask"], w["seq_id"], S,
+                         A.astype(np.float64), 0.2, 0.28, float(S), token_weighted, ref=ref.astype(np.float64),
+                         beta=beta)
+    assert int(res["status"].item()) == 0
+    sc = max(abs(o["loss"]), o["abs_terms"])
+    assert abs(float(res["loss"].item()) - o["loss"]) <= 1e-5 * sc
+    np.testing.assert_allclose(res["coef"].cpu().numpy(), o["coef"], rtol=1e-4, atol=1e-9)
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 5])
+def test_gspo_sequence_parallel(gpu_lib, R):
+    # the packed token sequence cut into R contiguous pieces at arbitrary
+    # token positions (documents span pieces); each piece computes its
+    # partials, the partials are gathered in piece order, and each piece
+    # finishes the loss and its own coefficients
+    import gspo_logprob_gb300 as g
+    cfg, w, logp, old, ref, A = _gspo_inputs()
+    S, N = cfg.num_docs, cfg.N
+    beta = 0.05
+    kw = dict(eps_low=0.2, eps_high=0.28, divisor=float(S), token_weighted=False, beta=beta)
+    whole = g.gspo_segment_loss(dev_tensor(logp), dev_tensor(old), dev_tensor(w["mask"]), dev_tensor(w["seq_id"]), S,
+                                dev_tensor(A), ref_logp=dev_tensor(ref), **kw)
+    cuts = [0] + sorted(np.random.default_rng(R).choice(np.arange(1, N), R - 1, replace=False).tolist()) + [N]
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        parts.append(g.gspo_segment_partials(dev_tensor(logp[a:b]), dev_tensor(old[a:b]), dev_tensor(w["mask"][a:b]),
+                                             dev_tensor(w["seq_id"][a:b]), S, ref_logp=dev_tensor(ref[a:b])))
+    fsum_all = torch.stack([p["fsum"] for p in parts])
+    cnt_all = torch.stack([p["cnt"] for p in parts])
+    coefs = []
+    losses = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        r = g.gspo_segment_loss_from_partials(dev_tensor(logp[a:b]), dev_tensor(w["mask"][a:b]),
+                                              dev_tensor(w["seq_id"][a:b]), S, fsum_all, cnt_all, dev_tensor(A),
+                                              ref_logp=dev_tensor(ref[a:b]), **kw)
+        assert int(r["status"].item()) == 0
+        coefs.append(r["coef"])
+        losses.append(r["loss"])
+    coef = torch.cat(coefs)
+    # every piece computes the same loss bits
+    for lo in losses[1:]:
+        assert torch.equal(lo.view(torch.int32), losses[0].view(torch.int32))
+    # integer counts are exact whatever the cut
+    counts = cnt_all[:, :S].sum(0).cpu().numpy()
+    valid = (w["seq_id"] >= 0) & (w["mask"] > 0)
+    np.testing.assert_array_equal(counts, np.bincount(w["seq_id"][valid], minlength=S))
+    if R == 1:
+        assert torch.equal(losses[0].view(torch.int32), whole["loss"].view(torch.int32))
+        assert torch.equal(coef.view(torch.int32), whole["coef"].view(torch.int32))
+    o = oracle.gspo_loss(logp.astype(np.float64), old.astype(np.float64), w["mask"], w["seq_id"], S,
+                         A.astype(np.float64), 0.2, 0.28, float(S), ref=ref.astype(np.float64), beta=beta)
+    sc = max(abs(o["loss"]), o["abs_terms"])
+    assert abs(float(losses[0].item()) - o["loss"]) <= 1e-5 * sc
+    np.testing.assert_allclose(coef.cpu().numpy(), o["coef"], rtol=1e-4, atol=1e-9)

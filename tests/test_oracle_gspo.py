@@ -122,3 +122,64 @@ def test_divisor_must_be_positive():
     with pytest.raises(oracle.OracleError):
         oracle.gspo_loss(np.zeros(2), np.zeros(2), np.ones(2, np.uint8), np.zeros(2, int), 1,
                          np.ones(1), 0.2, 0.2, 0.0)
+
+
+def test_kl_term_length_one_segments_equal_token_grpo():
+    # every token its own segment: the segment-mean KL is the token KL, so GSPO
+    # with beta and divisor C equals token-level GRPO with the fixed normaliser C
+    rng = np.random.default_rng(31)
+    N = 36
+    logp = -rng.uniform(0.1, 4, N)
+    old = logp + rng.uniform(-0.4, 0.4, N)
+    ref = logp + rng.uniform(-0.3, 0.3, N)
+    adv = rng.standard_normal(N)
+    mask = np.ones(N, dtype=np.uint8)
+    seg = np.arange(N)
+    g = oracle.gspo_loss(logp, old, mask, seg, N, adv, 0.2, 0.28, 11.0, ref=ref, beta=0.07)
+    t = oracle.grpo_loss(logp, old, ref, mask, seg, adv, N, 0.2, 0.28, 0.07, "fixed", 11.0)
+    assert abs(g["loss"] - t["loss"]) < 1e-14
+    np.testing.assert_allclose(g["coef"], t["coef"], atol=1e-15)
+
+
+def test_kl_term_zero_at_reference_and_nonnegative():
+    w = make_workload(CONFIGS[3], N=2048, with_weight=False, masked_frac=0.1)
+    rng = np.random.default_rng(32)
+    logp = -rng.uniform(0.1, 4, 2048)
+    old = logp + rng.uniform(-0.01, 0.01, 2048)
+    S = CONFIGS[3].num_docs
+    adv = rng.standard_normal(S)
+    base = oracle.gspo_loss(logp, old, w["mask"], w["seq_id"], S, adv, 0.2, 0.2, 48.0)
+    same = oracle.gspo_loss(logp, old, w["mask"], w["seq_id"], S, adv, 0.2, 0.2, 48.0, ref=logp, beta=0.5)
+    assert abs(same["loss"] - base["loss"]) < 1e-14
+    np.testing.assert_allclose(same["coef"], base["coef"], atol=1e-16)
+    ref = logp + rng.uniform(-0.3, 0.3, 2048)
+    kl = oracle.gspo_loss(logp, old, w["mask"], w["seq_id"], S, adv, 0.2, 0.2, 48.0, ref=ref, beta=0.5)
+    assert np.all(kl["seg_kl"] >= 0.0) and kl["loss"] >= base["loss"]
+
+
+def test_kl_term_coef_is_derivative():
+    rng = np.random.default_rng(33)
+    N, S = 50, 6
+    seg = np.sort(rng.integers(0, S, N))
+    seg[-3:] = -1
+    mask = (rng.random(N) < 0.85).astype(np.uint8)
+    mask[-3:] = 0
+    logp = -rng.uniform(0.1, 3, N)
+    old = logp + rng.uniform(-0.5, 0.5, N)
+    ref = logp + rng.uniform(-0.3, 0.3, N)
+    adv = rng.standard_normal(S)
+    for tw in (False, True):
+        args = (old, mask, seg, S, adv, 0.1, 0.15, 4.0, tw, ref, 0.3)
+        res = oracle.gspo_loss(logp, *args)
+        rho = res["seg_ratio"]
+        h = 1e-6
+        for i in range(N):
+            s = seg[i]
+            if s >= 0 and (abs(rho[s] - 0.9) < 1e-4 or abs(rho[s] - 1.15) < 1e-4):
+                continue
+            lp = logp.copy()
+            lp[i] += h
+            up = oracle.gspo_loss(lp, *args)["loss"]
+            lp[i] -= 2 * h
+            dn = oracle.gspo_loss(lp, *args)["loss"]
+            assert abs((up - dn) / (2 * h) - res["coef"][i]) < 1e-7
