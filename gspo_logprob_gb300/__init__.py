@@ -13,7 +13,8 @@ library is missing.
 """
 __all__ = ["grpo_head_forward", "gspo_segment_loss", "grpo_head_backward", "grpo_group_advantage",
            "grpo_loss_from_sequence_totals", "grpo_head_logprob_shard", "grpo_logprob_merge",
-           "vocab_shard_bounds", "gspo_segment_partials", "gspo_segment_loss_from_partials", "build", "ops"]
+           "vocab_shard_bounds", "gspo_segment_partials", "gspo_segment_loss_from_partials",
+           "grpo_head_backward_shard", "grpo_dh_merge", "build", "ops"]
 
 
 def build(verbose: bool = False) -> str:
@@ -24,7 +25,8 @@ def build(verbose: bool = False) -> str:
 def __getattr__(name):
     if name in ("grpo_head_forward", "gspo_segment_loss", "grpo_head_backward", "grpo_group_advantage",
                 "grpo_loss_from_sequence_totals", "grpo_head_logprob_shard", "grpo_logprob_merge",
-                "vocab_shard_bounds", "gspo_segment_partials", "gspo_segment_loss_from_partials", "ops"):
+                "vocab_shard_bounds", "gspo_segment_partials", "gspo_segment_loss_from_partials",
+                "grpo_head_backward_shard", "grpo_dh_merge", "ops"):
         import importlib
         ops = importlib.import_module(".ops", __name__)
         return ops if name == "ops" else getattr(ops, name)

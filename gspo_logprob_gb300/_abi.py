@@ -22,7 +22,7 @@ GH_BF16, GH_FP32 = 0, 1
 GH_TOKEN_MEAN, GH_SEQ_MEAN, GH_FIXED = 0, 1, 2
 REDUCTIONS = {"token_mean": GH_TOKEN_MEAN, "seq_mean": GH_SEQ_MEAN, "fixed": GH_FIXED}
 RATIO_LEVELS = {"token": 0, "sequence": 1}
-NUM_KERNEL_KINDS = 16
+NUM_KERNEL_KINDS = 17
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # GH_NOALLOC_SCRATCH_BYTES
 
 
@@ -63,6 +63,9 @@ SIGNATURES = {
                                           c_void_p]),
     "grpo_logprob_merge": (c_int32, [c_int64, c_int64, c_int32, POINTER(c_int64), c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "grpo_head_backward_shard": (c_int32, [POINTER(GhHead), c_int64, c_int64, c_void_p, c_void_p, c_void_p,
+                                           c_void_p, c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "grpo_dh_merge": (c_int32, [c_int32, c_int64, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "grpo_loss_from_sequence_totals": (c_int32, [c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_double, c_float,
                                                  c_void_p, c_void_p, c_void_p]),
     "gh_status_string": (c_char_p, [c_int32]),

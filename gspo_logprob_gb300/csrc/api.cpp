@@ -237,7 +237,7 @@ using namespace gh;
 
 extern "C" {
 
-int32_t gh_abi_version(void) { return 102; }
+int32_t gh_abi_version(void) { return 103; }
 
 const char* gh_status_string(gh_status s) {
   switch (s) {
@@ -502,12 +502,12 @@ gh_status gspo_segment_loss_from_partials(int64_t N, const float* logp, const fl
   return GH_OK;
 }
 
-gh_status grpo_head_backward(const gh_head* head, const float* lse, const float* coef, const float* grad_out,
-                             void* dH, float* dW, int32_t accumulate_dW, int32_t* status, void* ws, size_t ws_bytes,
-                             void* stream) {
-  g_last_error.clear();
-  gh_status s = check_head(head);
-  if (s != GH_OK) return s;
+// Backward body shared by the whole-vocabulary and the vocabulary-shard
+// entry points.  col_offset: global id of local column 0 (targets are global).
+// dh_partial: dH is an fp32 [N, D] partial over this vocabulary (no cast).
+static gh_status backward_impl(const gh_head* head, const float* lse, const float* coef, const float* grad_out,
+                               void* dH, float* dW, int32_t accumulate_dW, int32_t* status, void* ws,
+                               size_t ws_bytes, void* stream, int col_offset, bool dh_partial) {
   if (!status || !dW) return fail(GH_ERR_INVALID_ARG, "status/dW is NULL");
   if (head->N > 0 && (!lse || !coef || !dH)) return fail(GH_ERR_INVALID_ARG, "lse/coef/dH is NULL");
   if (!aligned16(dW) || (head->N > 0 && !aligned16(dH))) return fail(GH_ERR_INVALID_ARG, "dH/dW must be 16-byte aligned");
@@ -532,19 +532,25 @@ gh_status grpo_head_backward(const gh_head* head, const float* lse, const float*
     const int ldg = static_cast<int>(w.vb);
     cudaError_t e;
     if (head->dtype == GH_BF16) {
-      TcDlogitsArgs da{N, D, V, vb0, width, ldg, head->H, head->W, head->targets, lse, coef, grad_out, w.G, status};
+      TcDlogitsArgs da{N, D, V, vb0, width, ldg, head->H, head->W, head->targets, lse, coef, grad_out, w.G, status,
+                       col_offset};
       e = run(K_DLOGITS_TC, st, [&] { return launch_dlogits_tc(da, st); });
       if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
       int mode;
-      if (w.nblk == 1)
+      float* acc32 = w.acc32;
+      if (dh_partial) {
+        mode = b == 0 ? 0 : 1;  // fp32 partial accumulated in place
+        acc32 = static_cast<float*>(dH);
+      } else if (w.nblk == 1) {
         mode = 3;
-      else if (b == 0)
+      } else if (b == 0) {
         mode = 0;
-      else if (b == w.nblk - 1)
+      } else if (b == w.nblk - 1) {
         mode = 2;
-      else
+      } else {
         mode = 1;
-      TcDhArgs ha{N, D, V, vb0, width, ldg, w.G, head->W, mode, w.acc32, dH, status};
+      }
+      TcDhArgs ha{N, D, V, vb0, width, ldg, w.G, head->W, mode, acc32, dH, status};
       e = run(K_DH_TC, st, [&] { return launch_dh_tc(ha, st); });
       if (e != cudaSuccess) return cuda_fail(e, "dH launch");
       TcDwArgs wa{N, D, V, vb0, width, ldg, w.G, head->H, accumulate_dW, dW, status};
@@ -554,7 +560,7 @@ gh_status grpo_head_backward(const gh_head* head, const float* lse, const float*
       const float* H = static_cast<const float*>(head->H);
       const float* W = static_cast<const float*>(head->W);
       float* G = static_cast<float*>(w.G);
-      F32DlogitsArgs da{N, D, V, vb0, width, ldg, H, W, head->targets, lse, coef, grad_out, G};
+      F32DlogitsArgs da{N, D, V, vb0, width, ldg, H, W, head->targets, lse, coef, grad_out, G, col_offset};
       e = run(K_DLOGITS_F32, st, [&] { return launch_dlogits_f32(da, st); });
       if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
       const int real = static_cast<int>((V - vb0) < width ? (V - vb0) : width);
@@ -569,6 +575,46 @@ gh_status grpo_head_backward(const gh_head* head, const float* lse, const float*
       if (e != cudaSuccess) return cuda_fail(e, "dW launch");
     }
   }
+  return GH_OK;
+}
+
+gh_status grpo_head_backward(const gh_head* head, const float* lse, const float* coef, const float* grad_out,
+                             void* dH, float* dW, int32_t accumulate_dW, int32_t* status, void* ws, size_t ws_bytes,
+                             void* stream) {
+  g_last_error.clear();
+  gh_status s = check_head(head);
+  if (s != GH_OK) return s;
+  return backward_impl(head, lse, coef, grad_out, dH, dW, accumulate_dW, status, ws, ws_bytes, stream, 0, false);
+}
+
+gh_status grpo_head_backward_shard(const gh_head* head, int64_t vocab_start, int64_t V_total, const float* lse,
+                                   const float* coef, const float* grad_out, float* dH_partial, float* dW,
+                                   int32_t accumulate_dW, int32_t* status, void* ws, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  gh_status s = check_head(head);
+  if (s != GH_OK) return s;
+  if (vocab_start < 0 || vocab_start % SPLIT_COLS != 0)
+    return fail(GH_ERR_INVALID_ARG, "vocab_start=%lld must be a multiple of %d", (long long)vocab_start, SPLIT_COLS);
+  if (V_total > (int64_t(1) << 28) || vocab_start + head->V > V_total)
+    return fail(GH_ERR_INVALID_ARG, "shard exceeds V_total");
+  return backward_impl(head, lse, coef, grad_out, dH_partial, dW, accumulate_dW, status, ws, ws_bytes, stream,
+                       static_cast<int>(vocab_start), true);
+}
+
+gh_status grpo_dh_merge(int32_t num_shards, int64_t N, int64_t D, int32_t dtype, const float* dH_partials, void* dH,
+                        int32_t* status, void* stream) {
+  g_last_error.clear();
+  if (!status || (N > 0 && (!dH_partials || !dH))) return fail(GH_ERR_INVALID_ARG, "a pointer is NULL");
+  if (num_shards < 1 || num_shards > MAX_SHARDS) return fail(GH_ERR_INVALID_ARG, "num_shards out of range");
+  if (N < 0 || D < 1 || N * D > (int64_t(1) << 40)) return fail(GH_ERR_INVALID_ARG, "N/D out of range");
+  if (dtype != GH_BF16 && dtype != GH_FP32) return fail(GH_ERR_INVALID_ARG, "dtype unknown");
+  if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = run(K_DH_MERGE, st, [&] {
+    return launch_dh_merge(num_shards, static_cast<size_t>(N) * static_cast<size_t>(D), dtype == GH_BF16,
+                           dH_partials, dH, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "dH merge launch");
   return GH_OK;
 }
 
@@ -617,7 +663,7 @@ const char* gh_kernel_kind_name(int32_t kind) {
   static const char* names[GH_NUM_KERNEL_KINDS] = {
       "fwd_logits_lse_tc", "merge_lse", "grpo_loss", "gspo_segment", "dlogits_tc", "dh_gemm_tc",
       "dw_gemm_tc", "group_advantage", "fwd_logits_lse_f32", "dlogits_f32", "gemm_f32", "timeout_probe",
-      "grpo_sequence_totals", "merge_lse_shards", "gspo_partials", "gspo_finish"};
+      "grpo_sequence_totals", "merge_lse_shards", "gspo_partials", "gspo_finish", "dh_merge"};
   if (kind < 0 || kind >= GH_NUM_KERNEL_KINDS) return "";
   return names[kind];
 }

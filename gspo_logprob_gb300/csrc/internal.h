@@ -41,6 +41,7 @@ enum KernelKind {
   K_MERGE_SHARDS = 13,
   K_GSPO_PARTIALS = 14,
   K_GSPO_FINISH = 15,
+  K_DH_MERGE = 16,
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -191,6 +192,9 @@ cudaError_t launch_gspo_finish(const GspoArgs& g, int R, const float* fsum_all, 
                                cudaStream_t st);
 cudaError_t launch_advantage(const float* rewards, int num_seqs, int group_size, float eps, float* adv,
                              cudaStream_t st);
+// dH = sum over shards (in shard order) of the fp32 partials [num_shards, n]
+cudaError_t launch_dh_merge(int num_shards, size_t n, bool to_bf16, const float* partials, void* out,
+                            cudaStream_t st);
 cudaError_t launch_timeout_probe(int* status, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace gh

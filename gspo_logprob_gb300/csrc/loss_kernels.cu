@@ -3,7 +3,10 @@
 // bounded-wait self-test.  All sums run in a fixed order (lane-strided partial
 // sums in token order, then a xor butterfly or a fixed shared-memory tree), so
 // results are deterministic without floating-point atomics.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -620,6 +623,20 @@ __global__ void advantage_kernel(const float* rewards, int num_seqs, int group_s
     adv[static_cast<size_t>(g) * group_size + k] = static_cast<float>((r[k] - mean) / (sd + eps));
 }
 
+// ---------------------------------------------------------------- dH shard merge
+__global__ void dh_merge_kernel(int num_shards, size_t n, bool to_bf16, const float* __restrict__ partials,
+                                void* out) {
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float v = 0.f;
+    for (int r = 0; r < num_shards; ++r) v += partials[static_cast<size_t>(r) * n + i];
+    if (to_bf16)
+      static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+    else
+      static_cast<float*>(out)[i] = v;
+  }
+}
+
 // ---------------------------------------------------------------- timeout probe
 __global__ void timeout_probe_kernel(int* status, uint64_t timeout_ns) {
   __shared__ uint64_t bar;
@@ -767,6 +784,14 @@ cudaError_t launch_advantage(const float* rewards, int num_seqs, int group_size,
   if (groups <= 0) return cudaSuccess;
   advantage_kernel<<<static_cast<unsigned>(ceil_div(groups, 128)), 128, 0, st>>>(rewards, num_seqs, group_size, eps,
                                                                                  adv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dh_merge(int num_shards, size_t n, bool to_bf16, const float* partials, void* out,
+                            cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((n + 255) / 256, 152 * 16));
+  dh_merge_kernel<<<blocks, 256, 0, st>>>(num_shards, n, to_bf16, partials, out);
   return cudaGetLastError();
 }
 

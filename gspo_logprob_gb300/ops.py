@@ -212,6 +212,46 @@ def grpo_logprob_merge(part_m, part_s, zy, shard_starts, targets, mask, *, V_tot
     return dict(logp=logp, lse=lse, status=st)
 
 
+def grpo_head_backward_shard(H, W_shard, targets, mask, lse, coef, *, vocab_start: int, V_total: int,
+                             grad_out=None, dW=None, accumulate_dW: bool = False, row_tile: int = 0,
+                             status: Optional[torch.Tensor] = None):
+    """One vocabulary shard's backward: dW for the shard's rows and the fp32
+    dH partial G_shard W_shard (sum the shards' partials with grpo_dh_merge)."""
+    head = make_head(H, W_shard, targets, mask, row_tile)
+    dev = H.device
+    N, D, V = head.N, head.D, head.V
+    _need(lse, "lse", _F32, (N,))
+    _need(coef, "coef", _F32, (N,))
+    dHp = torch.empty(N, D, dtype=_F32, device=dev)
+    if dW is None:
+        if accumulate_dW:
+            raise ValueError("accumulate_dW needs an existing dW")
+        dW = torch.empty(V, D, dtype=_F32, device=dev)
+    else:
+        _need(dW, "dW", _F32, (V, D))
+    st = new_status(dev) if status is None else status
+    nbytes = backward_workspace_bytes(head)
+    ws = WORKSPACE.get(dev, nbytes)
+    code = _lib().grpo_head_backward_shard(ctypes.byref(head), int(vocab_start), int(V_total), _ptr(lse), _ptr(coef),
+                                           _ptr(grad_out), _ptr(dHp), _ptr(dW), 1 if accumulate_dW else 0, _ptr(st),
+                                           _ptr(ws), nbytes, _stream(dev))
+    _abi.check(code, "grpo_head_backward_shard")
+    return dict(dH_partial=dHp, dW=dW, status=st)
+
+
+def grpo_dh_merge(dH_partials, dtype=torch.bfloat16, status: Optional[torch.Tensor] = None):
+    """dH = sum over shards (in order) of the gathered fp32 partials [P, N, D]."""
+    P, N, D = dH_partials.shape
+    _need(dH_partials, "dH_partials", _F32)
+    dev = dH_partials.device
+    dH = torch.empty(N, D, dtype=dtype, device=dev)
+    st = new_status(dev) if status is None else status
+    code = _lib().grpo_dh_merge(P, N, D, _abi.GH_BF16 if dtype == _BF16 else _abi.GH_FP32, _ptr(dH_partials),
+                                _ptr(dH), _ptr(st), _stream(dev))
+    _abi.check(code, "grpo_dh_merge")
+    return dH
+
+
 def grpo_loss_from_sequence_totals(seq_policy, seq_kl, seq_count, *, reduction: str = "token_mean",
                                    norm: float = 0.0, beta: float = 0.0, status: Optional[torch.Tensor] = None):
     """(loss, policy_loss, kl) from per-sequence totals gathered in global

@@ -183,6 +183,28 @@ gh_status grpo_logprob_merge(int64_t N, int64_t V_total, int32_t num_shards, con
                              const uint8_t* mask, float* logp, float* lse, int32_t* status, void* stream);
 
 /*
+ * Backward of one vocabulary shard (the tensor-parallel counterpart of
+ * grpo_head_backward): head->W is the shard holding global columns
+ * [vocab_start, vocab_start + head->V); lse and coef are the full-vocabulary
+ * per-row values (from grpo_logprob_merge and the loss), identical on every
+ * rank.  Writes dW [head->V, D] fp32 for the shard's rows (added to dW when
+ * accumulate_dW) and dH_partial [N, D] fp32 = G_shard W_shard; the shards'
+ * partials summed in shard order (grpo_dh_merge) give dH.  Workspace: at least
+ * grpo_head_backward_workspace_size(head) bytes.
+ */
+gh_status grpo_head_backward_shard(const gh_head* head, int64_t vocab_start, int64_t V_total, const float* lse,
+                                   const float* coef, const float* grad_out, float* dH_partial, float* dW,
+                                   int32_t accumulate_dW, int32_t* status, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dH [N, D] (in dtype) = sum over shards, in shard order, of the gathered fp32
+ * partials dH_partials [num_shards, N, D] (a deterministic reduction in place
+ * of a float all-reduce).
+ */
+gh_status grpo_dh_merge(int32_t num_shards, int64_t N, int64_t D, int32_t dtype, const float* dH_partials, void* dH,
+                        int32_t* status, void* stream);
+
+/*
  * (loss, policy_loss, kl) from per-sequence totals gathered across
  * data-parallel ranks (RL-Kernel PR #291, Key Changes: Reference Op: each rank
  * owns whole sequences; per-sequence totals are all-gathered as a
@@ -307,9 +329,9 @@ int32_t gh_abi_version(void);
  * Kinds: 0 fwd logits+LSE, 1 merge, 2 GRPO loss, 3 GSPO loss, 4 dlogits,
  * 5 dH GEMM, 6 dW GEMM, 7 advantage, 8 fp32 forward, 9 fp32 dlogits,
  * 10 fp32 GEMM, 11 timeout probe, 12 GRPO loss from sequence totals, 13 shard merge,
- * 14 GSPO partials, 15 GSPO loss from partials.
+ * 14 GSPO partials, 15 GSPO loss from partials, 16 dH shard merge.
  */
-#define GH_NUM_KERNEL_KINDS 16
+#define GH_NUM_KERNEL_KINDS 17
 void gh_profile_enable(int32_t on);
 void gh_profile_reset(void);
 gh_status gh_profile_read(int32_t kind, int64_t* launches, double* total_ms);

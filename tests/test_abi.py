@@ -60,7 +60,7 @@ def test_struct_layout_matches_c(lib, tmp_path):
 
 
 def test_host_only_calls(lib):
-    assert lib.gh_abi_version() == 102
+    assert lib.gh_abi_version() == 103
     assert lib.gh_status_string(0) == b"GH_OK"
     assert lib.gh_status_string(3) == b"GH_ERR_WORKSPACE"
     assert lib.gh_kernel_kind_name(0) == b"fwd_logits_lse_tc"

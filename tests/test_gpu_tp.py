@@ -79,3 +79,38 @@ def test_tp_out_of_range_targets(gpu_lib):
     assert st & 1                           # GH_DEV_TARGET_OOR
     lp = merged["logp"].cpu().numpy()
     assert math.isnan(lp[7]) and lp[8] == 0.0
+
+
+@pytest.mark.parametrize("P", [2, 4])
+def test_tp_backward(gpu_lib, P):
+    # vocabulary-parallel backward: each shard's dlogits use the full-vocabulary
+    # LSE and coef; dW rows come out bitwise equal to the single-shard backward,
+    # dH is the shard-ordered sum of fp32 partials (fp32 rounding of that sum
+    # differs from one accumulation), checked against the oracle
+    import gspo_logprob_gb300 as g
+    from gpu_helpers import assert_grad_bf16, bf16_np, dev_tensor
+    cfg = CONFIGS[2]
+    w = make_workload(cfg)
+    H, W = host_head(w)
+    lp, lse, _ = oracle.selected_logprob(H, W, w["targets"], w["mask"])
+    old = (lp + w["u_old"]).astype(np.float32)
+    ref = (lp + w["u_ref"]).astype(np.float32)
+    adv = oracle.group_advantages(w["rewards"], w["group_size"]).astype(np.float32)
+    Hd, Wd, y, m = dev_head(w)
+    V = cfg.V
+    fw = g.grpo_head_forward(Hd, Wd, y, m, old_logp=dev_tensor(old), ref_logp=dev_tensor(ref), adv=dev_tensor(adv),
+                             seq_id=dev_tensor(w["seq_id"]), num_seqs=w["num_seqs"], eps_low=cfg.eps_low,
+                             eps_high=cfg.eps_high, beta=cfg.beta)
+    whole = g.grpo_head_backward(Hd, Wd, y, m, fw["lse"], fw["coef"])
+    bounds = g.vocab_shard_bounds(V, P)
+    parts = [g.grpo_head_backward_shard(Hd, Wd[s:s + n], y, m, fw["lse"], fw["coef"], vocab_start=s, V_total=V)
+             for s, n in bounds]
+    dW = torch.cat([p["dW"] for p in parts])
+    dH = g.grpo_dh_merge(torch.stack([p["dH_partial"] for p in parts]))
+    torch.cuda.synchronize()
+    assert all(int(p["status"].item()) == 0 for p in parts)
+    assert torch.equal(dW.view(torch.int32), whole["dW"].view(torch.int32))
+    o = oracle.forward_backward(H, W, w["targets"], w["mask"], w["seq_id"], adv.astype(np.float64), w["num_seqs"],
+                                old.astype(np.float64), ref.astype(np.float64), cfg.eps_low, cfg.eps_high, cfg.beta)
+    assert_grad_bf16(bf16_np(dH), o["dH"], "dH (tensor parallel)")
+    assert_grad_bf16(bf16_np(whole["dH"]), bf16_np(dH), "dH tp vs single")
