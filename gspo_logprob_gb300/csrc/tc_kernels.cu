@@ -4,6 +4,7 @@
 
 #include "internal.h"
 #include "tc_gemm.cuh"
+#include "tc_gemm_pair.cuh"
 
 namespace gh {
 
@@ -58,11 +59,11 @@ int dlogits_group_m() {
   return v;
 }
 int dh_group_m() {
-  static const int v = kind_group_m("GH_DH_GROUP_M", 4);
+  static const int v = kind_group_m("GH_DH_GROUP_M", 16);
   return v;
 }
 int dw_group_m() {
-  static const int v = kind_group_m("GH_DW_GROUP_M", 4);
+  static const int v = kind_group_m("GH_DW_GROUP_M", 16);
   return v;
 }
 
@@ -80,6 +81,84 @@ cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const TcSche
   if (sc.num_tasks <= 0) return cudaSuccess;
   const int grid = static_cast<int>(sc.num_tasks < num_sms() ? sc.num_tasks : num_sms());
   kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, sc, b_off_n, b_off_k, ep, status, timeout_ns());
+  return cudaGetLastError();
+}
+
+// CTA-pair kernels (cta_group::2, 256 x 256 tiles over two SMs) per kind: 1 on
+// (default; measured faster for every kind on the 8B-vocabulary workload), 0 the
+// single-CTA kernels selected by the tile-height knobs below
+int pair_knob(const char* name, int dflt) {
+  const int v = env_int(name, dflt);
+  return v == 0 || v == 1 ? v : dflt;
+}
+int fwd_pair() {
+  static const int v = pair_knob("GH_FWD_PAIR", 1);
+  return v;
+}
+int dlogits_pair() {
+  static const int v = pair_knob("GH_DLOGITS_PAIR", 1);
+  return v;
+}
+int dh_pair() {
+  static const int v = pair_knob("GH_DH_PAIR", 1);
+  return v;
+}
+int dw_pair() {
+  static const int v = pair_knob("GH_DW_PAIR", 1);
+  return v;
+}
+
+int max_pairs() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) cache[dev] = num_sms() / 2 > 0 ? num_sms() / 2 : 1;
+  return cache[dev];
+}
+
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const TcSched& sc, int b_off_n, int b_off_k,
+                           const typename Epi::Params& ep, int* status, cudaStream_t st) {
+  using C = TcPairCfg;
+  auto kern = tc_gemm_pair_kernel<A_MN, B_MN, Epi>;
+  static bool attr_set = false;  // per instantiation
+  static int pairs_fit = 0;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(2 * max_pairs());
+    q.blockDim = dim3(C::THREADS);
+    q.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = 2;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    q.attrs = qa;
+    q.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) n = max_pairs();
+    pairs_fit = n < max_pairs() ? n : max_pairs();
+    attr_set = true;
+  }
+  if (sc.num_tasks <= 0) return cudaSuccess;
+  const int pairs = sc.num_tasks < pairs_fit ? sc.num_tasks : pairs_fit;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, sc, b_off_n, b_off_k, ep, status, timeout_ns());
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -123,6 +202,12 @@ cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st) {
   }
   const int num_m = static_cast<int>(ceil_div(a.N, 2 * TC_BM));
   TcSched sc = make_sched(num_m, num_vt, TILES_PER_SPLIT, nkb, 2 * TC_BM, num_m);
+  if (fwd_pair()) {
+    CUtensorMap tb2;  // each CTA of the pair stages 128 of the 256 columns
+    if (!make_tmap_bf16(&tb2, a.W, a.D, a.V, static_cast<uint64_t>(a.D) * 2, TC_BK, TC_BN / 2))
+      return cudaErrorInvalidValue;
+    return launch_tc_pair<false, false, EpiFwdLse>(ta, tb2, sc, 0, 0, ep, a.status, st);
+  }
   return launch_tc<2, 1, false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);
 }
 
@@ -148,6 +233,12 @@ cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st) {
     return launch_tc<1, 1, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
   }
   TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dlogits_group_m());
+  if (dlogits_pair()) {
+    CUtensorMap tb2;
+    if (!make_tmap_bf16(&tb2, a.W, a.D, a.V, static_cast<uint64_t>(a.D) * 2, TC_BK, TC_BN / 2))
+      return cudaErrorInvalidValue;
+    return launch_tc_pair<false, false, EpiDlogits>(ta, tb2, sc, a.vb0, 0, ep, a.status, st);
+  }
   if (dlogits_cg() == 2) return launch_tc<2, 2, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
   return launch_tc<2, 1, false, false, EpiDlogits>(ta, tb, sc, a.vb0, 0, ep, a.status, st);
 }
@@ -167,6 +258,10 @@ cudaError_t launch_dh_tc(const TcDhArgs& a, cudaStream_t st) {
   ep.out16 = static_cast<__nv_bfloat16*>(a.out16);
   const int nkb = static_cast<int>(ceil_div(a.width, TC_BK));
   const int nn = static_cast<int>(ceil_div(a.D, TC_BN));
+  if (dh_pair()) {
+    TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dh_group_m());
+    return launch_tc_pair<false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
+  }
   if (dh_mt() == 1) {
     TcSched sc = make_sched(static_cast<int>(ceil_div(a.N, TC_BM)), nn, 1, nkb, TC_BM, dh_group_m());
     return launch_tc<1, 1, false, true, EpiStore>(ta, tb, sc, 0, a.vb0, ep, a.status, st);
@@ -193,6 +288,10 @@ cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st) {
   ep.out16 = nullptr;
   const int nkb = static_cast<int>(ceil_div(a.N, TC_BK));
   const int nn = static_cast<int>(ceil_div(a.D, TC_BN));
+  if (dw_pair()) {
+    TcSched sc = make_sched(static_cast<int>(ceil_div(rows, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dw_group_m());
+    return launch_tc_pair<true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
+  }
   if (dw_mt() == 1) {
     TcSched sc = make_sched(static_cast<int>(ceil_div(rows, TC_BM)), nn, 1, nkb, TC_BM, dw_group_m());
     return launch_tc<1, 1, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);

@@ -55,6 +55,12 @@ def main(dtype):
     else:
         assert np.max(np.abs(bw["dH"].cpu().numpy() - o["dH"])) <= 2e-4
         assert np.max(np.abs(bw["dW"].cpu().numpy() - o["dW"])) <= 2e-4
+    # the row tile (and with it the kernel variant) must not change a bit
+    ref = g.grpo_head_forward(Hd, Wd, y, m, row_tile=128)
+    for rt in (0, 64, 256):
+        o2 = g.grpo_head_forward(Hd, Wd, y, m, row_tile=rt)
+        assert torch.equal(o2["lse"].view(torch.int32), ref["lse"].view(torch.int32)), rt
+        assert torch.equal(o2["logp"].view(torch.int32), ref["logp"].view(torch.int32)), rt
     print("ok", dtype, e)
 
 

@@ -16,9 +16,17 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 SETTINGS = [
     {"GH_BWD_BLOCK_COLS": "512"},                                  # 6 blocks: dH store / add / add+cast
-    {"GH_BWD_BLOCK_COLS": "1024", "GH_DH_MT": "2", "GH_DLOGITS_MT": "1", "GH_DW_MT": "1"},
+    {"GH_BWD_BLOCK_COLS": "512", "GH_FWD_PAIR": "0", "GH_DLOGITS_PAIR": "0", "GH_DH_PAIR": "0", "GH_DW_PAIR": "0"},
+    {"GH_BWD_BLOCK_COLS": "1024", "GH_DH_MT": "2", "GH_DLOGITS_MT": "1", "GH_DW_MT": "1", "GH_DLOGITS_PAIR": "0",
+     "GH_DH_PAIR": "0", "GH_DW_PAIR": "0"},
     {"GH_BWD_BLOCK_COLS": "768", "GH_DLOGITS_GROUP_M": "1", "GH_DH_GROUP_M": "3", "GH_DW_GROUP_M": "64"},
-    {"GH_BWD_BLOCK_COLS": "1280", "GH_DH_MT": "2", "GH_DH_CG": "2", "GH_DW_CG": "2", "GH_DLOGITS_CG": "2"},
+    {"GH_BWD_BLOCK_COLS": "768", "GH_DLOGITS_GROUP_M": "1", "GH_DH_GROUP_M": "3", "GH_DW_GROUP_M": "64",
+     "GH_DLOGITS_PAIR": "0", "GH_DH_PAIR": "0", "GH_DW_PAIR": "0"},
+    {"GH_BWD_BLOCK_COLS": "1280", "GH_DH_MT": "2", "GH_DH_CG": "2", "GH_DW_CG": "2", "GH_DLOGITS_CG": "2",
+     "GH_DLOGITS_PAIR": "0", "GH_DH_PAIR": "0", "GH_DW_PAIR": "0"},
+    {"GH_FWD_PAIR": "1", "GH_DLOGITS_PAIR": "1", "GH_DH_PAIR": "1", "GH_DW_PAIR": "1", "GH_BWD_BLOCK_COLS": "1024"},
+    {"GH_FWD_PAIR": "0", "GH_DLOGITS_PAIR": "0", "GH_DH_PAIR": "0", "GH_DW_PAIR": "0"},
+    {"GH_FWD_PAIR": "0", "GH_DLOGITS_PAIR": "1", "GH_DH_PAIR": "0", "GH_DW_PAIR": "1", "GH_BWD_BLOCK_COLS": "768"},
 ]
 
 
