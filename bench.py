@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--micro-batches", type=int, default=None, help="override (testing only)")
-    ap.add_argument("--cpu-rows", type=int, default=96, help="tokens in the oracle's timed sample")
+    ap.add_argument("--cpu-rows", type=int, default=384,
+                    help="tokens in the oracle's timed sample (about 10-20 s of host work on 16 cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -400,7 +401,7 @@ def run_reference(args, rank, world):
     cfg = CONFIGS[4]
     host_masks = [make_workload(cfg, micro_batch=k, with_weight=False)["mask"] for k in range(cfg.micro_batches)]
     norm = float(sum(int(x.sum()) for x in host_masks))
-    rows = max(8, args.cpu_rows // 2)
+    rows = max(8, args.cpu_rows // 4)
     for _ in range(max(0, min(args.warmup, 1))):
         oracle_sample(cfg, 8, norm)
     times = []
