@@ -47,10 +47,6 @@ enum KernelKind {
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-struct TmapPair {
-  CUtensorMap a, b;
-};
-
 // bf16 2-D tensor map (row-major [outer, inner], row stride in bytes), 128-byte
 // swizzle, zero fill out of bounds.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

@@ -89,3 +89,41 @@ def test_gspo_full_size_sampled_rows(gpu_lib):
     assert int(fw["status"].item()) == 0
     assert np.max(np.abs(fw["logp"].cpu().numpy()[rows] - lp_s)) <= BF16_LOGP_ABS
     assert np.max(np.abs(fw["lse"].cpu().numpy()[rows] - lse_s)) <= BF16_LOGP_ABS
+
+
+def test_gspo_full_size_end_to_end(gpu_lib):
+    # the whole packed-GSPO workload (N=16384, D=2048, V=32000), forward, loss
+    # and backward, element by element against the fp64 oracle
+    import gspo_logprob_gb300 as g
+    from gpu_helpers import BF16_LOSS_REL, host_head
+    cfg = CONFIGS[3]
+    w = make_workload(cfg, masked_frac=0.1)
+    H, W = host_head(w)
+    lp_o, lse_o, _ = oracle.selected_logprob(H, W, w["targets"], w["mask"])
+    old = (lp_o + w["u_old"]).astype(np.float32)
+    A = oracle.group_advantages(w["rewards"], w["group_size"]).astype(np.float32)
+    S = cfg.num_docs
+    o = oracle.gspo_loss(lp_o, old.astype(np.float64), w["mask"], w["seq_id"], S, A.astype(np.float64),
+                         cfg.eps_low, cfg.eps_high, float(S))
+    dH_o, dW_o = oracle.head_backward(H, W, w["targets"], lse_o, o["coef"])
+    Hd, Wd, y, m = dev_head(w)
+    fw = g.grpo_head_forward(Hd, Wd, y, m)
+    gs = g.gspo_segment_loss(fw["logp"], dev_tensor(old), m, dev_tensor(w["seq_id"]), S, dev_tensor(A),
+                             eps_low=cfg.eps_low, eps_high=cfg.eps_high, divisor=float(S))
+    bw = g.grpo_head_backward(Hd, Wd, y, m, fw["lse"], gs["coef"])
+    torch.cuda.synchronize()
+    assert int(fw["status"].item()) == 0 and int(gs["status"].item()) == 0 and int(bw["status"].item()) == 0
+    assert np.max(np.abs(fw["logp"].cpu().numpy() - lp_o)) <= BF16_LOGP_ABS
+    assert np.max(np.abs(fw["lse"].cpu().numpy() - lse_o)) <= BF16_LOGP_ABS
+    sc = max(abs(o["loss"]), o["abs_terms"])
+    assert abs(float(gs["loss"].item()) - o["loss"]) <= BF16_LOSS_REL * sc
+    rho = o["seg_ratio"]
+    near = (np.abs(rho - (1 - cfg.eps_low)) < 2e-5) | (np.abs(rho - (1 + cfg.eps_high)) < 2e-5)
+    if not near.any():
+        assert_grad_bf16(bf16_np(bw["dH"]), dH_o, "dH")
+        assert_grad_bf16(bw["dW"].cpu().numpy(), dW_o, "dW")
+    else:
+        # a segment at a clip edge switches its gradient on or off: compare the
+        # rows of documents away from the edges
+        keep = np.array([s < 0 or not near[s] for s in w["seq_id"]])
+        assert_grad_bf16(bf16_np(bw["dH"])[keep], dH_o[keep], "dH (rows away from clip edges)")
