@@ -38,6 +38,17 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused GRPO head fwd+bwd tokens/sec; TFLOPS as % of GB300 dense BF16 peak"
+# Secondary workloads: name -> (workload index in synth.CONFIGS, storage dtype, what a step runs)
+AUX_WORKLOADS = {
+    "gspo_packed": (3, "bf16", "fwd+gspo+bwd"),
+    "grpo_small": (2, "bf16", "fwd+grpo+bwd"),
+    "selective_logp_bf16": (1, "bf16", "fwd"),
+    "selective_logp_f32": (1, "fp32", "fwd"),
+    "grpo_small_f32": (2, "fp32", "fwd+grpo+bwd"),
+}
+# fp32 FMA peak of the SIMT twin: 152 SMs x 128 fp32 lanes x 2 FLOP x 2070 MHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+L2_FLUSH_BYTES = 512 << 20
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 
@@ -53,6 +64,9 @@ def parse():
                     help="tokens in the oracle's timed sample (about 10-20 s of host work on 16 cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["grpo_8b_vocab"] + sorted(AUX_WORKLOADS), default="grpo_8b_vocab",
+                    help="grpo_8b_vocab (default) is the headline step; the others measure the remaining paths "
+                         "(one GPU, L2 flushed between timed steps)")
     return ap.parse_args()
 
 
@@ -392,6 +406,164 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- secondary workloads
+def oracle_sample_aux(cfg, w, dt: str, what: str, rows: int):
+    """The fp64 oracle on `rows` tokens of workload `cfg` (the same inputs the
+    GPU leg runs): logits + LSE, and for the loss workloads the loss over the
+    whole batch plus the sampled rows' dH / dW contributions."""
+    import numpy as np
+
+    import oracle
+    W = oracle.as_f64(w["W"], dt)
+    H = oracle.as_f64(w["H"][:rows], dt)
+    y, m, seq = w["targets"][:rows], w["mask"][:rows], w["seq_id"][:rows]
+    t0 = time.perf_counter()
+    lp, lse, _ = oracle.selected_logprob(H, W, y, m)
+    if what != "fwd":
+        adv = oracle.group_advantages(w["rewards"], w["group_size"])
+        if cfg.kind == "gspo":
+            lp_all = np.full(cfg.N, -math.log(cfg.V))
+            lp_all[:rows] = lp
+            res = oracle.gspo_loss(lp_all, lp_all + w["u_old"], w["mask"], w["seq_id"], cfg.num_docs, adv,
+                                   cfg.eps_low, cfg.eps_high, float(cfg.num_docs))
+            coef = res["coef"][:rows]
+        else:
+            res = oracle.grpo_loss(lp, lp + w["u_old"][:rows], lp + w["u_ref"][:rows], m, seq, adv, w["num_seqs"],
+                                   cfg.eps_low, cfg.eps_high, cfg.beta, "token_mean")
+            coef = res["coef"]
+        oracle.head_backward(H, W, y, lse, coef)
+    dt_s = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    desc = f"{rows} of {cfg.N} tokens, full V={cfg.V} and D={cfg.D}: fp64 {what.replace('+', ', ')} (numpy/OpenBLAS)"
+    return rows / dt_s, dt_s, cores, desc
+
+
+def run_aux(args, rank, world, local):
+    """One GPU: the workload `args.workload` names, each timed step bracketed by
+    CUDA events and followed (outside the events) by an L2 flush."""
+    import numpy as np
+    import torch
+
+    import gspo_logprob_gb300 as g
+    from gspo_logprob_gb300 import ops
+    from synth import CONFIGS, make_workload
+
+    if world > 1:
+        raise SystemExit("secondary workloads run on one GPU")
+    idx, dt, what = AUX_WORKLOADS[args.workload]
+    cfg = CONFIGS[idx]
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    g.build()
+    w = make_workload(cfg, dtype=dt)
+    N, D, V = cfg.N, cfg.D, cfg.V
+
+    def mat(x):
+        a = torch.from_numpy(np.ascontiguousarray(x))
+        return (a.view(torch.int16).view(torch.bfloat16) if dt == "bf16" else a).to(dev)
+
+    H, W = mat(w["H"]), mat(w["W"])
+    y, m = (torch.from_numpy(w[k]).to(dev) for k in ("targets", "mask"))
+    seq = torch.from_numpy(w["seq_id"]).to(dev)
+    status = ops.new_status(dev)
+    out = dict(logp=torch.empty(N, device=dev), lse=torch.empty(N, device=dev))
+    if what != "fwd":
+        lp0 = g.grpo_head_forward(H, W, y, m)["logp"]
+        old = lp0 + torch.from_numpy(w["u_old"]).to(dev).float()
+        ref = lp0 + torch.from_numpy(w["u_ref"]).to(dev).float()
+        rew = torch.from_numpy(w["rewards"]).to(dev)
+        G, S = w["group_size"], w["num_seqs"]
+        dH = torch.empty(N, D, dtype=H.dtype, device=dev)
+        dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+        out.update(coef=torch.empty(N, device=dev), loss3=torch.empty(3, device=dev))
+
+    def step():
+        if what == "fwd":
+            g.grpo_head_forward(H, W, y, m, status=status, out=out)
+            return
+        adv = g.grpo_group_advantage(rew, G, status=status)
+        if cfg.kind == "gspo":
+            fw = g.grpo_head_forward(H, W, y, m, status=status, out=out)
+            coef = g.gspo_segment_loss(fw["logp"], old, m, seq, S, adv, eps_low=cfg.eps_low, eps_high=cfg.eps_high,
+                                       divisor=float(S), status=status)["coef"]
+        else:
+            fw = g.grpo_head_forward(H, W, y, m, old_logp=old, ref_logp=ref, adv=adv, seq_id=seq, num_seqs=S,
+                                     eps_low=cfg.eps_low, eps_high=cfg.eps_high, beta=cfg.beta, status=status,
+                                     out=out)
+            coef = fw["coef"]
+        g.grpo_head_backward(H, W, y, m, fw["lse"], coef, dH=dH, dW=dW, status=status)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    ops.raise_on_status(status)
+    clocks = ClockSampler(local)
+    clocks.start()
+    ops.profile_reset()
+    ops.profile_enable(True)
+    n0 = ops.launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        step()
+        b.record()
+        flush.zero_()
+    torch.cuda.synchronize()
+    launches = ops.launch_count() - n0
+    ops.profile_enable(False)
+    prof = ops.profile_read()
+    clk = clocks.stop()
+    ops.raise_on_status(status)
+    ms_step = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    passes = {"fwd": 1, "fwd+grpo+bwd": 4, "fwd+gspo+bwd": 4}[what]
+    flops_step = 2.0 * passes * N * D * V
+    burst, _, hbm, src = measured_peaks()
+    if dt == "bf16":
+        alg = {k: 2.0 * N * D * V for k in ("fwd_logits_lse_tc", "dlogits_tc", "dh_gemm_tc", "dw_gemm_tc")}
+        bound, peak, peak_src = "tensor", burst, f"{src} bf16_tflops (burst: a short step timed alone)"
+    else:
+        alg = {"fwd_logits_lse_f32": 2.0 * N * D * V, "dlogits_f32": 2.0 * N * D * V, "gemm_f32": 4.0 * N * D * V}
+        bound, peak = "alu", FP32_ALU_TFLOPS
+        peak_src = "152 SMs x 128 fp32 lanes x 2 FLOP (FMA) x 2070 MHz maximum SM clock"
+    kernels = {}
+    for name, (n, tot) in prof.items():
+        per_step_ms = tot / args.steps
+        ent = {"launches_per_step": n / args.steps, "ms_per_step": round(per_step_ms, 5),
+               "avg_launch_us": round(1e3 * tot / n, 2), "share": round(per_step_ms / ms_step, 4)}
+        if name in alg:
+            ent["tflops"] = round(alg[name] / (per_step_ms * 1e-3) / 1e12, 2)
+        kernels[name] = ent
+    dom = max((k for k in kernels if k in alg), key=lambda k: kernels[k]["ms_per_step"])
+    roof = {"kernel": dom, "bound": bound, "achieved": kernels[dom]["tflops"], "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(kernels[dom]["tflops"] / peak, 4), "traffic": None,
+            "algorithmic_flops_per_launch": alg[dom] / kernels[dom]["launches_per_step"], "peak_source": peak_src}
+    res = {
+        "metric": METRIC, "value": round(N / (ms_step * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dt == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {cfg.name}, N={N}, D={D}, V={V}, step = {what}",
+                   "l2": "flushed between timed steps (512 MB write outside the events)"},
+        "tflops": round(flops_step / (ms_step * 1e-3) / 1e12, 2), "roofline": roof, "kernels": kernels,
+        "gpu_launches": launches, "clocks": clk, "e2e": None,
+    }
+    if "gspo_segment" in kernels:
+        nbytes = N * (4 + 4 + 1 + 4 + 4) + 8 * w["num_seqs"]
+        us = kernels["gspo_segment"]["avg_launch_us"]
+        res["gspo_seam"] = {"us_per_launch": us, "algorithmic_bytes": nbytes,
+                            "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1), "hbm_peak_GB_per_s": hbm,
+                            "bound": "latency (one launch over %d KB)" % (nbytes // 1024)}
+    if not args.no_cpu_baseline:
+        rows = {1: N, 2: N, 3: 256}[idx]
+        tps, secs, cores, desc = oracle_sample_aux(cfg, w, dt, what, rows)
+        res["cpu_baseline"] = {"value": round(tps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "sample": desc, "seconds": round(secs, 2)}
+    print(json.dumps(res), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands, on the host cores, on bounded samples of the
     same workload (rank 0 only)."""
@@ -426,6 +598,9 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.workload != "grpo_8b_vocab":
+        run_aux(args, rank, world, local)
         return
     run_ours(args, rank, world, local)
 

@@ -23,7 +23,7 @@ GH_TOKEN_MEAN, GH_SEQ_MEAN, GH_FIXED = 0, 1, 2
 REDUCTIONS = {"token_mean": GH_TOKEN_MEAN, "seq_mean": GH_SEQ_MEAN, "fixed": GH_FIXED}
 RATIO_LEVELS = {"token": 0, "sequence": 1}
 NUM_KERNEL_KINDS = 17
-NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # GH_NOALLOC_SCRATCH_BYTES
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # GH_NOALLOC_SCRATCH_BYTES
 
 
 class GhHead(ctypes.Structure):
@@ -59,6 +59,7 @@ SIGNATURES = {
     "grpo_head_forward_noalloc": (c_int32, [POINTER(GhHead), POINTER(GhGrpo), c_void_p, c_void_p, c_void_p,
                                             c_void_p, c_void_p, c_void_p]),
     "gh_vocab_shard_bounds": (c_int32, [c_int64, c_int32, c_int32, POINTER(c_int64), POINTER(c_int64)]),
+    "gh_vocab_splits": (c_int64, [c_int64]),
     "grpo_head_logprob_shard": (c_int32, [POINTER(GhHead), c_int64, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
                                           c_void_p]),
     "grpo_logprob_merge": (c_int32, [c_int64, c_int64, c_int32, POINTER(c_int64), c_void_p, c_void_p, c_void_p,

@@ -237,7 +237,7 @@ using namespace gh;
 
 extern "C" {
 
-int32_t gh_abi_version(void) { return 103; }
+int32_t gh_abi_version(void) { return 104; }
 
 const char* gh_status_string(gh_status s) {
   switch (s) {
@@ -318,6 +318,8 @@ gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* log
   }
   return GH_OK;
 }
+
+int64_t gh_vocab_splits(int64_t V) { return V < 1 ? 0 : num_splits(V); }
 
 gh_status gh_vocab_shard_bounds(int64_t V_total, int32_t num_shards, int32_t rank, int64_t* start, int64_t* len) {
   g_last_error.clear();

@@ -10,12 +10,14 @@
 
 namespace gh {
 
-// Column tiling of the vocabulary: 256-column tiles, TILES_PER_SPLIT tiles per
-// split.  The split count depends on V only, which keeps logp/LSE bitwise
-// independent of N, the row tile and the GPU's SM count.
+// Column tiling of the vocabulary: 256-column tiles; each tile is one split,
+// whose per-row (max, sum exp) partial the merge folds in a fixed order.  The
+// split count depends on V only, which keeps logp/LSE bitwise independent of N,
+// the row tile, the task schedule and the GPU's SM count.
 constexpr int VTILE = 256;
-constexpr int TILES_PER_SPLIT = 4;
+constexpr int TILES_PER_SPLIT = 1;
 constexpr int SPLIT_COLS = VTILE * TILES_PER_SPLIT;
+static_assert(SPLIT_COLS == 256, "the fp32 logits kernels write one partial per 256-column tile");
 // Backward vocabulary block (columns of dlogits held in the workspace at once):
 // 16384 by default (fewer fp32 dH read-modify-write passes), or a multiple of
 // 256 from GH_BWD_BLOCK_COLS (a tuning knob; dW and the dlogits are the same

@@ -39,23 +39,52 @@ __device__ __forceinline__ int lower_bound_i(const int* key, int lo, int hi, int
 }
 
 // ---------------------------------------------------------------- merge
-// LSE_i = M + log(sum_k s_k e^{m_k - M}) over splits k in increasing order.
-__global__ void merge_kernel(int N, int V, int splits, const float* __restrict__ part_m,
-                             const float* __restrict__ part_s, const float* __restrict__ zy,
-                             const int* __restrict__ targets, const uint8_t* __restrict__ mask, float* logp,
-                             float* lse, int* status) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N) return;
-  float M = -INFINITY;
-  for (int k = 0; k < splits; ++k) M = fmaxf(M, part_m[static_cast<size_t>(k) * N + i]);
-  float S = 0.f;
-  if (M != -INFINITY) {
-    for (int k = 0; k < splits; ++k) {
+// LSE_i = M + log(sum_k s_k e^{m_k - M}) over the splits k (one per 256-column tile).
+// Fold of the split partials of rows blockIdx.x * 32 + lane (256 threads: warp
+// g = 0..7 is a split group, lane a row).  M = max over splits of part_m (exact
+// in any order); S = sum over splits of part_s * exp(part_m - M), where group g
+// sums the splits k = g, g + 8, g + 16, ... in increasing order and the eight
+// group sums are then added in group order.  The order depends on the split
+// count only (a function of V), never on N or on how the rows were batched.
+// Returns the LSE in warp 0's lanes (meaningless in the others).
+__device__ __forceinline__ float fold_splits(int N, int splits, const float* __restrict__ part_m,
+                                             const float* __restrict__ part_s, float (*red)[33]) {
+  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 32 + lane;
+  const bool ok = i < N;
+  float mx = -INFINITY;
+  if (ok)
+    for (int k = g; k < splits; k += 8) mx = fmaxf(mx, part_m[static_cast<size_t>(k) * N + i]);
+  red[g][lane] = mx;
+  __syncthreads();
+  float M = red[0][lane];
+#pragma unroll
+  for (int h = 1; h < 8; ++h) M = fmaxf(M, red[h][lane]);
+  __syncthreads();
+  float s = 0.f;
+  if (ok && M != -INFINITY) {
+    for (int k = g; k < splits; k += 8) {
       const float mk = part_m[static_cast<size_t>(k) * N + i];
-      if (mk != -INFINITY) S += part_s[static_cast<size_t>(k) * N + i] * expf(mk - M);
+      if (mk != -INFINITY) s += part_s[static_cast<size_t>(k) * N + i] * expf(mk - M);
     }
   }
-  const float L = M + logf(S);
+  red[g][lane] = s;
+  __syncthreads();
+  float S = red[0][lane];
+#pragma unroll
+  for (int h = 1; h < 8; ++h) S += red[h][lane];
+  return M + logf(S);
+}
+
+__global__ void __launch_bounds__(256) merge_kernel(int N, int V, int splits, const float* __restrict__ part_m,
+                                                    const float* __restrict__ part_s, const float* __restrict__ zy,
+                                                    const int* __restrict__ targets,
+                                                    const uint8_t* __restrict__ mask, float* logp, float* lse,
+                                                    int* status) {
+  __shared__ float red[8][33];
+  const float L = fold_splits(N, splits, part_m, part_s, red);
+  const int i = blockIdx.x * 32 + (threadIdx.x & 31);
+  if (threadIdx.x >= 32 || i >= N) return;
   lse[i] = L;
   const int y = targets[i];
   const bool act = mask[i] != 0;
@@ -75,22 +104,17 @@ __global__ void merge_kernel(int N, int V, int splits, const float* __restrict__
 // merge of vocabulary-parallel partials: the splits of all shards in global
 // order (the same fold as merge_kernel), the target logit from the shard that
 // owns the target column
-__global__ void merge_shards_kernel(int N, int V_total, int splits, const float* __restrict__ part_m,
-                                    const float* __restrict__ part_s, const float* __restrict__ zy,
-                                    const ShardBounds sb, const int* __restrict__ targets,
-                                    const uint8_t* __restrict__ mask, float* logp, float* lse, int* status) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N) return;
-  float M = -INFINITY;
-  for (int k = 0; k < splits; ++k) M = fmaxf(M, part_m[static_cast<size_t>(k) * N + i]);
-  float S = 0.f;
-  if (M != -INFINITY) {
-    for (int k = 0; k < splits; ++k) {
-      const float mk = part_m[static_cast<size_t>(k) * N + i];
-      if (mk != -INFINITY) S += part_s[static_cast<size_t>(k) * N + i] * expf(mk - M);
-    }
-  }
-  const float L = M + logf(S);
+__global__ void __launch_bounds__(256) merge_shards_kernel(int N, int V_total, int splits,
+                                                           const float* __restrict__ part_m,
+                                                           const float* __restrict__ part_s,
+                                                           const float* __restrict__ zy, const ShardBounds sb,
+                                                           const int* __restrict__ targets,
+                                                           const uint8_t* __restrict__ mask, float* logp, float* lse,
+                                                           int* status) {
+  __shared__ float red[8][33];
+  const float L = fold_splits(N, splits, part_m, part_s, red);
+  const int i = blockIdx.x * 32 + (threadIdx.x & 31);
+  if (threadIdx.x >= 32 || i >= N) return;
   lse[i] = L;
   const int y = targets[i];
   const bool act = mask[i] != 0;
@@ -660,8 +684,8 @@ cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const fl
                          const int32_t* targets, const uint8_t* mask, float* logp, float* lse, int* status,
                          cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
-  merge_kernel<<<static_cast<unsigned>(ceil_div(N, 256)), 256, 0, st>>>(N, V, splits, part_m, part_s, zy, targets,
-                                                                         mask, logp, lse, status);
+  merge_kernel<<<static_cast<unsigned>(ceil_div(N, 32)), 256, 0, st>>>(N, V, splits, part_m, part_s, zy, targets,
+                                                                        mask, logp, lse, status);
   return cudaGetLastError();
 }
 
@@ -669,8 +693,8 @@ cudaError_t launch_merge_shards(int N, int V_total, int splits, const float* par
                                 const float* zy, const ShardBounds& sb, const int32_t* targets, const uint8_t* mask,
                                 float* logp, float* lse, int* status, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
-  merge_shards_kernel<<<static_cast<unsigned>(ceil_div(N, 256)), 256, 0, st>>>(N, V_total, splits, part_m, part_s, zy,
-                                                                                sb, targets, mask, logp, lse, status);
+  merge_shards_kernel<<<static_cast<unsigned>(ceil_div(N, 32)), 256, 0, st>>>(N, V_total, splits, part_m, part_s, zy,
+                                                                               sb, targets, mask, logp, lse, status);
   return cudaGetLastError();
 }
 

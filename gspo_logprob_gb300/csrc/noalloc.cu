@@ -9,7 +9,7 @@
 // them grpo_head_forward_noalloc runs the same forward with its scratch in the
 // fixed device array below, so the caller only passes inputs and outputs.
 //
-// The array is GH_NOALLOC_SCRATCH_BYTES (16 MiB); every GPU that loads this
+// The array is GH_NOALLOC_SCRATCH_BYTES (64 MiB); every GPU that loads this
 // library holds it until the process exits.  Its device address is looked up
 // once per device (with that device current) on the first call made there, so
 // that first call should come before any stream capture.  All calls share the

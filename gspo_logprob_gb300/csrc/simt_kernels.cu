@@ -1,12 +1,17 @@
-// fp32 path (exact fp32 FMA on the CUDA cores, no TF32): logits + online LSE,
-// dlogits recompute and a plain tiled GEMM for dH / dW.
+// fp32 path (exact fp32 FMA on the CUDA cores, no TF32): logits + per-tile
+// (max, sum exp), dlogits recompute and the dH / dW GEMMs.
 //
-// Every logit z_ij is one fmaf chain over k = 0..D-1 in increasing order, so
-// its value does not depend on the tiling.  Per 256-column vocabulary tile a
-// warp owns 4 rows: lane l holds columns l + 32 j (j = 0..7); the tile max and
-// the tile sum of exp(z - M) are formed lane-locally in j order and then by a
-// xor butterfly (every lane ends with the same bits), and the running (m, s)
-// of each row is updated tile by tile in column order.
+// Every logit z_ij and every GEMM output is one fmaf chain over k = 0, 1, ...
+// in increasing order, so its value does not depend on the tiling or on which
+// CTA computes it.  The kernels are register tiled: a thread keeps an 8 x 8
+// block of outputs, operands are staged in shared memory (double buffered,
+// the next K chunk is fetched into registers while the current one is used).
+//
+// Logits tile (forward and dlogits): 64 rows x 256 columns (one vocabulary
+// tile) per 256-thread CTA.  Warp w owns rows 8w..8w+7; lane l owns columns
+// 4l..4l+3 and 128+4l..128+4l+3.  A row's tile max and sum of exp(z - max) are
+// formed lane-locally in column order and then by a xor butterfly, so every
+// lane ends with the same bits whatever the row tile.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -15,9 +20,9 @@ namespace gh {
 
 namespace {
 
-constexpr int F_ROWS = 32;   // rows per sub-block
-constexpr int F_KC = 32;     // K chunk
-constexpr int F_THREADS = 256;
+constexpr int L_BM = 64, L_BN = 256, L_BK = 16, L_THREADS = 256;
+constexpr int L_APAD = L_BM + 4;   // smem row stride of the H chunk (floats)
+constexpr int L_BPAD = L_BN + 4;   // smem row stride of the W chunk (floats)
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -30,229 +35,338 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// z[r][j] for rows r0 + warp*4 + r and columns c0 + lane + 32 j of one 256-wide tile
-__device__ __forceinline__ void f32_logits_tile(const float* __restrict__ H, const float* __restrict__ W, int N,
-                                                int D, int V, int r0, int c0, float (*Hs)[F_KC],
-                                                float (*Ws)[F_KC + 1], float z[4][8]) {
+// four consecutive floats p[0..3] of a row of length `len` starting at column
+// `c` (zero beyond len); vector load when aligned and in bounds
+template <bool VEC>
+__device__ __forceinline__ float4 load4(const float* __restrict__ row, int c, int len) {
+  if (VEC && c + 3 < len) return __ldg(reinterpret_cast<const float4*>(row + c));
+  float4 v;
+  v.x = c < len ? __ldg(row + c) : 0.f;
+  v.y = c + 1 < len ? __ldg(row + c + 1) : 0.f;
+  v.z = c + 2 < len ? __ldg(row + c + 2) : 0.f;
+  v.w = c + 3 < len ? __ldg(row + c + 3) : 0.f;
+  return v;
+}
+
+struct LogitsSmem {
+  float A[2][L_BK][L_APAD];  // H chunk, k-major: A[k][row]
+  float B[2][L_BK][L_BPAD];  // W chunk, k-major: B[k][col]
+};
+
+// Column of output j (0..7) of lane l within the 256-wide tile.
+__device__ __forceinline__ int lcol(int lane, int j) { return (j < 4 ? 4 * lane : 128 + 4 * lane) + (j & 3); }
+
+// z[r][j] = sum_k H[r0 + 8w + r, k] W[c0 + lcol(lane, j), k] (zero for rows >= N
+// or columns >= V).  Thread t fetches one float4 of H (row t/4, k 4(t%4)) and
+// four of W (column (t + 256q)/4) per K chunk.
+template <bool VEC>
+__device__ __forceinline__ void logits_tile(const float* __restrict__ H, const float* __restrict__ W, int N, int D,
+                                            int V, int r0, int c0, LogitsSmem& sm, float z[8][8]) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+  for (int r = 0; r < 8; ++r)
 #pragma unroll
     for (int j = 0; j < 8; ++j) z[r][j] = 0.f;
-  for (int k0 = 0; k0 < D; k0 += F_KC) {
-    __syncthreads();
-    for (int e = t; e < F_ROWS * F_KC; e += F_THREADS) {
-      const int r = e / F_KC, k = e % F_KC;
-      const int gr = r0 + r, gk = k0 + k;
-      Hs[r][k] = (gr < N && gk < D) ? H[static_cast<size_t>(gr) * D + gk] : 0.f;
+  const int ar = t >> 2, akq = (t & 3) * 4;
+  const int agr = r0 + ar;
+  const float* hrow = H + static_cast<size_t>(agr < N ? agr : 0) * D;
+  const float* wrow[4];
+  int bc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    bc[q] = (t + 256 * q) >> 2;
+    const int gc = c0 + bc[q];
+    wrow[q] = W + static_cast<size_t>(gc < V ? gc : 0) * D;
+  }
+  const bool arow_ok = agr < N;
+  bool bcol_ok[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) bcol_ok[q] = c0 + bc[q] < V;
+
+  float4 pa, pb[4];
+  auto fetch = [&](int k0) {
+    pa = arow_ok ? load4<VEC>(hrow, k0 + akq, D) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      pb[q] = bcol_ok[q] ? load4<VEC>(wrow[q], k0 + akq, D) : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto stash = [&](int buf) {
+    sm.A[buf][akq + 0][ar] = pa.x;
+    sm.A[buf][akq + 1][ar] = pa.y;
+    sm.A[buf][akq + 2][ar] = pa.z;
+    sm.A[buf][akq + 3][ar] = pa.w;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      sm.B[buf][akq + 0][bc[q]] = pb[q].x;
+      sm.B[buf][akq + 1][bc[q]] = pb[q].y;
+      sm.B[buf][akq + 2][bc[q]] = pb[q].z;
+      sm.B[buf][akq + 3][bc[q]] = pb[q].w;
     }
-    for (int e = t; e < 256 * F_KC; e += F_THREADS) {
-      const int c = e / F_KC, k = e % F_KC;
-      const int gc = c0 + c, gk = k0 + k;
-      Ws[c][k] = (gc < V && gk < D) ? W[static_cast<size_t>(gc) * D + gk] : 0.f;
+  };
+
+  const int nk = (D + L_BK - 1) / L_BK;
+  __syncthreads();  // the previous tile's readers of sm are done
+  fetch(0);
+  stash(0);
+  __syncthreads();
+  for (int kc = 0; kc < nk; ++kc) {
+    const int buf = kc & 1;
+    if (kc + 1 < nk) fetch((kc + 1) * L_BK);
+#pragma unroll
+    for (int k = 0; k < L_BK; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&sm.A[buf][k][warp * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&sm.A[buf][k][warp * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&sm.B[buf][k][4 * lane]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&sm.B[buf][k][128 + 4 * lane]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) z[r][j] = fmaf(a[r], b[j], z[r][j]);
     }
-    __syncthreads();
-    const int kmax = (D - k0) < F_KC ? (D - k0) : F_KC;
-    for (int k = 0; k < kmax; ++k) {
-      float h[4], w[8];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) h[r] = Hs[warp * 4 + r][k];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = Ws[lane + 32 * j][k];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) z[r][j] = fmaf(h[r], w[j], z[r][j]);
+    if (kc + 1 < nk) {
+      stash(buf ^ 1);
+      __syncthreads();
     }
   }
 }
 
-// grid: (num_row_groups, splits); each CTA walks the row group's 32-row
-// sub-blocks and, for each, the split's vocabulary tiles in order.
-__global__ void __launch_bounds__(F_THREADS) f32_fwd_kernel(const float* __restrict__ H, const float* __restrict__ W,
-                                                           const int* __restrict__ targets, int N, int D, int V,
-                                                           int row_tile, int col_offset, float* part_m,
-                                                           float* part_s, float* zy) {
-  __shared__ float Hs[F_ROWS][F_KC];
-  __shared__ float Ws[256][F_KC + 1];
+// grid: (ceil(N / row_tile), vocabulary tiles).  A CTA walks its row tile in
+// 64-row sub-blocks; for each row it writes the tile's (max, sum exp(z - max))
+// as the split partial and, where the target falls in the tile, z_y.
+template <bool VEC>
+__global__ void __launch_bounds__(L_THREADS, 2) f32_fwd_kernel(const float* __restrict__ H,
+                                                              const float* __restrict__ W,
+                                                              const int* __restrict__ targets, int N, int D, int V,
+                                                              int row_tile, int col_offset, float* part_m,
+                                                              float* part_s, float* zy) {
+  __shared__ __align__(16) LogitsSmem sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.y;
-  const int num_vt = (V + 255) / 256;
-  const int t_begin = split * TILES_PER_SPLIT;
-  const int t_end = min(num_vt, t_begin + TILES_PER_SPLIT);
-  for (int sb = 0; sb < row_tile / F_ROWS; ++sb) {
-    const int r0 = blockIdx.x * row_tile + sb * F_ROWS;
+  const int c0 = split * L_BN;
+  for (int sb = 0; sb < row_tile / L_BM; ++sb) {
+    const int r0 = blockIdx.x * row_tile + sb * L_BM;
     if (r0 >= N) break;
-    float m[4], s[4];
-    int y[4];
+    float z[8][8];
+    logits_tile<VEC>(H, W, N, D, V, r0, c0, sm, z);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      m[r] = -INFINITY;
-      s[r] = 0.f;
-      const int gr = r0 + warp * 4 + r;
-      y[r] = gr < N ? targets[gr] - col_offset : -1;  // local column of the target
-    }
-    for (int vt = t_begin; vt < t_end; ++vt) {
-      const int c0 = vt * 256;
-      float z[4][8];
-      f32_logits_tile(H, W, N, D, V, r0, c0, Hs, Ws, z);
+    for (int r = 0; r < 8; ++r) {
+      const int gr = r0 + warp * 8 + r;
+      const int y = gr < N ? __ldg(targets + gr) - col_offset : -1;  // local column of the target
+      float lm = -INFINITY;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int gr = r0 + warp * 4 + r;
-        float lm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int col = c0 + lane + 32 * j;
-          if (col == y[r] && gr < N) zy[gr] = z[r][j];
-          if (col >= V) z[r][j] = -INFINITY;
-          lm = fmaxf(lm, z[r][j]);
-        }
-        const float tmax = warp_max(lm);
-        if (tmax == -INFINITY) continue;
-        const float mnew = fmaxf(m[r], tmax);
+      for (int j = 0; j < 8; ++j) {
+        const int col = c0 + lcol(lane, j);
+        if (col == y) zy[gr] = z[r][j];
+        if (col >= V) z[r][j] = -INFINITY;
+        lm = fmaxf(lm, z[r][j]);
+      }
+      const float tmax = warp_max(lm);
+      float tsum = 0.f;
+      if (tmax != -INFINITY) {
         float ls = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ls += expf(z[r][j] - mnew);
-        const float tsum = warp_sum(ls);
-        s[r] = (m[r] == -INFINITY ? 0.f : s[r] * expf(m[r] - mnew)) + tsum;
-        m[r] = mnew;
+        for (int j = 0; j < 8; ++j) ls += expf(z[r][j] - tmax);
+        tsum = warp_sum(ls);
       }
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int gr = r0 + warp * 4 + r;
-        if (gr < N) {
-          part_m[static_cast<size_t>(split) * N + gr] = m[r];
-          part_s[static_cast<size_t>(split) * N + gr] = s[r];
-        }
+      if (lane == 0 && gr < N) {
+        part_m[static_cast<size_t>(split) * N + gr] = tmax;
+        part_s[static_cast<size_t>(split) * N + gr] = tsum;
       }
     }
   }
 }
 
-// grid: (ceil(N/32), width/256)
-__global__ void __launch_bounds__(F_THREADS) f32_dlogits_kernel(const float* __restrict__ H,
-                                                               const float* __restrict__ W,
-                                                               const int* __restrict__ targets,
-                                                               const float* __restrict__ lse,
-                                                               const float* __restrict__ coef,
-                                                               const float* __restrict__ grad_out, int N, int D,
-                                                               int V, int vb0, int ldg, int col_offset, float* G) {
-  __shared__ float Hs[F_ROWS][F_KC];
-  __shared__ float Ws[256][F_KC + 1];
+// grid: (ceil(N / 64), width / 256).  G[i, lc] = g coef_i (1[col = y_i] - exp(z - LSE_i))
+// for the block's local column lc (0 at padded columns).
+template <bool VEC>
+__global__ void __launch_bounds__(L_THREADS, 2) f32_dlogits_kernel(
+    const float* __restrict__ H, const float* __restrict__ W, const int* __restrict__ targets,
+    const float* __restrict__ lse, const float* __restrict__ coef, const float* __restrict__ grad_out, int N, int D,
+    int V, int vb0, int ldg, int col_offset, float* G) {
+  __shared__ __align__(16) LogitsSmem sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blockIdx.x * F_ROWS;
-  const int lc0 = blockIdx.y * 256;
+  const int r0 = blockIdx.x * L_BM;
+  const int lc0 = blockIdx.y * L_BN;
   const int c0 = vb0 + lc0;
-  float z[4][8];
-  f32_logits_tile(H, W, N, D, V, r0, c0, Hs, Ws, z);
+  float z[8][8];
+  logits_tile<VEC>(H, W, N, D, V, r0, c0, sm, z);
   const float g = grad_out ? *grad_out : 1.f;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int gr = r0 + warp * 4 + r;
+  for (int r = 0; r < 8; ++r) {
+    const int gr = r0 + warp * 8 + r;
     if (gr >= N) continue;
     const float sc = g * coef[gr];
     const float L = lse[gr];
     const int y = targets[gr] - col_offset;
+    float o[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int col = c0 + lane + 32 * j;
+      const int col = c0 + lcol(lane, j);
       const float p = col < V ? expf(z[r][j] - L) : 0.f;
-      G[static_cast<size_t>(gr) * ldg + lc0 + lane + 32 * j] = sc * ((col == y ? 1.f : 0.f) - p);
+      o[j] = sc * ((col == y ? 1.f : 0.f) - p);
     }
+    float* grow = G + static_cast<size_t>(gr) * ldg + lc0;
+    *reinterpret_cast<float4*>(grow + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4*>(grow + 128 + 4 * lane) = make_float4(o[4], o[5], o[6], o[7]);
   }
 }
 
-constexpr int GT = 64, GK = 16;
+// ---------------------------------------------------------------- GEMM
+// C[row_off + m, n] (+)= sum_k A(m, k) B(k, n) with B n-contiguous (B(k, n) =
+// B[k sbk + n]) and A either k-contiguous (A(m, k) = A[m sam + k]: dH = G W)
+// or m-contiguous (A(m, k) = A[m + k sak]: dW = G^T H).  128 x 128 tile per
+// 256-thread CTA; thread (tr, tc) = (t / 16, t % 16) owns rows 4tr.., 64+4tr..
+// and columns 4tc.., 64+4tc...
+constexpr int G_BM = 128, G_BN = 128, G_BK = 16;
+constexpr int G_PAD = G_BM + 4;
 
-__global__ void __launch_bounds__(256) f32_gemm_kernel(F32GemmArgs a) {
-  __shared__ float As[GK][GT + 4];
-  __shared__ float Bs[GK][GT + 4];
+template <bool A_KCONTIG, bool VEC>
+__global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
+  __shared__ __align__(16) float As[2][G_BK][G_PAD];
+  __shared__ __align__(16) float Bs[2][G_BK][G_PAD];
   const int t = threadIdx.x;
-  const int tm = t / 16, tn = t % 16;  // 16 x 16 threads, 4 x 4 outputs each
-  const int m0 = blockIdx.y * GT, n0 = blockIdx.x * GT;
-  float acc[4][4];
+  const int tr = t >> 4, tc = t & 15;
+  const int m0 = blockIdx.y * G_BM, n0 = blockIdx.x * G_BN;
+  float acc[8][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < a.K; k0 += GK) {
-    __syncthreads();
-    for (int e = t; e < GK * GT; e += 256) {
-      int m, k;
-      if (a.sak == 1) {
-        k = e % GK;
-        m = e / GK;
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  float4 pa[2], pb[2];
+  // A chunk: 128 x 16.  k-contiguous: element e = t + 256q -> row e/4, k 4(e%4).
+  // m-contiguous: e -> k e/32, rows 4(e%32)..
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int e = t + 256 * q;
+      if (A_KCONTIG) {
+        const int m = e >> 2, kq = (e & 3) * 4;
+        const int gm = m0 + m;
+        pa[q] = gm < a.M ? load4<VEC>(a.A + static_cast<long long>(gm) * a.sam, k0 + kq, a.K)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
       } else {
-        m = e % GT;
-        k = e / GT;
+        const int k = e >> 5, mq = (e & 31) * 4;
+        const int gk = k0 + k;
+        pa[q] = gk < a.K ? load4<VEC>(a.A + static_cast<long long>(gk) * a.sak, m0 + mq, a.M)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      const int gm = m0 + m, gk = k0 + k;
-      As[k][m] = (gm < a.M && gk < a.K) ? a.A[gm * a.sam + gk * a.sak] : 0.f;
-      int n, kb;
-      if (a.sbn == 1) {
-        n = e % GT;
-        kb = e / GT;
-      } else {
-        kb = e % GK;
-        n = e / GK;
-      }
-      const int gn = n0 + n, gkb = k0 + kb;
-      Bs[kb][n] = (gn < a.Nn && gkb < a.K) ? a.B[gkb * a.sbk + gn * a.sbn] : 0.f;
+      const int k = e >> 5, nq = (e & 31) * 4;
+      const int gk = k0 + k;
+      pb[q] = gk < a.K ? load4<VEC>(a.B + static_cast<long long>(gk) * a.sbk, n0 + nq, a.Nn)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
-    const int kmax = (a.K - k0) < GK ? (a.K - k0) : GK;
-    for (int k = 0; k < kmax; ++k) {
-      float av[4], bv[4];
+  };
+  auto stash = [&](int buf) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = As[k][tm + 16 * i];
+    for (int q = 0; q < 2; ++q) {
+      const int e = t + 256 * q;
+      if (A_KCONTIG) {
+        const int m = e >> 2, kq = (e & 3) * 4;
+        As[buf][kq + 0][m] = pa[q].x;
+        As[buf][kq + 1][m] = pa[q].y;
+        As[buf][kq + 2][m] = pa[q].z;
+        As[buf][kq + 3][m] = pa[q].w;
+      } else {
+        const int k = e >> 5, mq = (e & 31) * 4;
+        *reinterpret_cast<float4*>(&As[buf][k][mq]) = pa[q];
+      }
+      const int k = e >> 5, nq = (e & 31) * 4;
+      *reinterpret_cast<float4*>(&Bs[buf][k][nq]) = pb[q];
+    }
+  };
+
+  const int nk = (a.K + G_BK - 1) / G_BK;
+  fetch(0);
+  stash(0);
+  __syncthreads();
+  for (int kc = 0; kc < nk; ++kc) {
+    const int buf = kc & 1;
+    if (kc + 1 < nk) fetch((kc + 1) * G_BK);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Bs[k][tn + 16 * j];
+    for (int k = 0; k < G_BK; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * tr]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][64 + 4 * tr]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][4 * tc]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][64 + 4 * tc]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (kc + 1 < nk) {
+      stash(buf ^ 1);
+      __syncthreads();
     }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int gm = m0 + tm + 16 * i;
+  for (int i = 0; i < 8; ++i) {
+    const int gm = m0 + (i < 4 ? 4 * tr : 64 + 4 * tr) + (i & 3);
     if (gm >= a.M) continue;
+    float* crow = a.C + (static_cast<long long>(a.row_off) + gm) * a.ldc;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int gn = n0 + tn + 16 * j;
+    for (int j = 0; j < 8; ++j) {
+      const int gn = n0 + (j < 4 ? 4 * tc : 64 + 4 * tc) + (j & 3);
       if (gn >= a.Nn) continue;
-      float* c = a.C + (static_cast<long long>(a.row_off) + gm) * a.ldc + gn;
-      *c = a.accumulate ? (*c + acc[i][j]) : acc[i][j];
+      crow[gn] = a.accumulate ? (crow[gn] + acc[i][j]) : acc[i][j];
     }
   }
 }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
 cudaError_t launch_fwd_f32(const F32FwdArgs& a, cudaStream_t st) {
-  const int rt = (a.row_tile == 64 || a.row_tile == 256) ? a.row_tile : 128;
-  const int splits = static_cast<int>(ceil_div(ceil_div(a.V, VTILE), TILES_PER_SPLIT));
-  dim3 grid(static_cast<unsigned>(ceil_div(a.N, rt)), static_cast<unsigned>(splits));
   if (a.N <= 0) return cudaSuccess;
-  f32_fwd_kernel<<<grid, F_THREADS, 0, st>>>(a.H, a.W, a.targets, a.N, a.D, a.V, rt, a.col_offset, a.part_m, a.part_s,
-                                              a.zy);
+  const int rt = (a.row_tile == 128 || a.row_tile == 256) ? a.row_tile : L_BM;
+  dim3 grid(static_cast<unsigned>(ceil_div(a.N, rt)), static_cast<unsigned>(ceil_div(a.V, VTILE)));
+  const bool vec = a.D % 4 == 0 && aligned16(a.H) && aligned16(a.W);
+  if (vec)
+    f32_fwd_kernel<true><<<grid, L_THREADS, 0, st>>>(a.H, a.W, a.targets, a.N, a.D, a.V, rt, a.col_offset, a.part_m,
+                                                      a.part_s, a.zy);
+  else
+    f32_fwd_kernel<false><<<grid, L_THREADS, 0, st>>>(a.H, a.W, a.targets, a.N, a.D, a.V, rt, a.col_offset,
+                                                       a.part_m, a.part_s, a.zy);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>(ceil_div(a.N, F_ROWS)), static_cast<unsigned>(ceil_div(a.width, 256)));
   if (a.N <= 0) return cudaSuccess;
-  f32_dlogits_kernel<<<grid, F_THREADS, 0, st>>>(a.H, a.W, a.targets, a.lse, a.coef, a.grad_out, a.N, a.D, a.V,
-                                                  a.vb0, a.ldg, a.col_offset, a.G);
+  if (a.width % L_BN != 0 || a.ldg % 4 != 0 || !aligned16(a.G)) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(ceil_div(a.N, L_BM)), static_cast<unsigned>(a.width / L_BN));
+  const bool vec = a.D % 4 == 0 && aligned16(a.H) && aligned16(a.W);
+  if (vec)
+    f32_dlogits_kernel<true><<<grid, L_THREADS, 0, st>>>(a.H, a.W, a.targets, a.lse, a.coef, a.grad_out, a.N, a.D,
+                                                          a.V, a.vb0, a.ldg, a.col_offset, a.G);
+  else
+    f32_dlogits_kernel<false><<<grid, L_THREADS, 0, st>>>(a.H, a.W, a.targets, a.lse, a.coef, a.grad_out, a.N, a.D,
+                                                           a.V, a.vb0, a.ldg, a.col_offset, a.G);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_f32(const F32GemmArgs& a, cudaStream_t st) {
   if (a.M <= 0 || a.Nn <= 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>(ceil_div(a.Nn, GT)), static_cast<unsigned>(ceil_div(a.M, GT)));
-  f32_gemm_kernel<<<grid, 256, 0, st>>>(a);
+  if (a.sbn != 1 || (a.sak != 1 && a.sam != 1)) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(ceil_div(a.Nn, G_BN)), static_cast<unsigned>(ceil_div(a.M, G_BM)));
+  const bool kc = a.sak == 1;
+  const long long lda = kc ? a.sam : a.sak;
+  const bool vec = aligned16(a.A) && aligned16(a.B) && lda % 4 == 0 && a.sbk % 4 == 0;
+  if (kc) {
+    if (vec)
+      f32_gemm_kernel<true, true><<<grid, 256, 0, st>>>(a);
+    else
+      f32_gemm_kernel<true, false><<<grid, 256, 0, st>>>(a);
+  } else {
+    if (vec)
+      f32_gemm_kernel<false, true><<<grid, 256, 0, st>>>(a);
+    else
+      f32_gemm_kernel<false, false><<<grid, 256, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

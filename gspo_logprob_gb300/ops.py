@@ -159,7 +159,7 @@ def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=
 
 
 def vocab_shard_bounds(V_total: int, num_shards: int):
-    """[(start, length)] of each vocabulary shard: whole 1024-column splits,
+    """[(start, length)] of each vocabulary shard: whole 256-column splits,
     the remainder spread over the first shards (host-only library call)."""
     lib = _lib()
     out = []
@@ -178,7 +178,7 @@ def grpo_head_logprob_shard(H, W_shard, targets, mask, *, vocab_start: int, V_to
     head = make_head(H, W_shard, targets, mask, row_tile)
     dev = H.device
     N = head.N
-    splits = -(-(-(-head.V // 256)) // 4)
+    splits = int(_lib().gh_vocab_splits(head.V))
     part_m = torch.empty(splits, N, dtype=_F32, device=dev)
     part_s = torch.empty(splits, N, dtype=_F32, device=dev)
     zy = torch.zeros(N, dtype=_F32, device=dev)
@@ -195,6 +195,9 @@ def grpo_logprob_merge(part_m, part_s, zy, shard_starts, targets, mask, *, V_tot
     order) and the shards' zy rows [num_shards, N]; shard_starts has
     num_shards + 1 host integers."""
     S, N = part_m.shape
+    if S != int(_lib().gh_vocab_splits(int(V_total))):
+        raise ValueError(f"part_m has {S} split rows; a {V_total}-column vocabulary has "
+                         f"{int(_lib().gh_vocab_splits(int(V_total)))}")
     _need(part_m, "part_m", _F32)
     _need(part_s, "part_s", _F32, (S, N))
     num_shards = len(shard_starts) - 1

@@ -150,24 +150,32 @@ gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* log
  * masked before the local (max, sumexp) partials; partials are moved by
  * all-gather and merged in fixed global shard order; cross-degree bitwise
  * equality needs a tile decomposition that does not depend on the number of
- * shards.  Here the decomposition is the global grid of 1024-column splits:
- * shard bounds are multiples of 1024 (gh_vocab_shard_bounds gives an even
+ * shards.  Here the decomposition is the global grid of 256-column splits:
+ * shard bounds are multiples of 256 (gh_vocab_shard_bounds gives an even
  * split), every shard's splits are global splits, and the merged result is
  * bitwise the one grpo_head_forward gives on the whole vocabulary.
  *
  * gh_vocab_shard_bounds: columns [*start, *start + *len) of shard `rank` of
  * `num_shards` over V_total (whole splits, the remainder spread over the first
- * shards; num_shards <= ceil(V_total / 1024)).  Host only.
+ * shards; num_shards <= ceil(V_total / 256)).  Host only.
  */
 gh_status gh_vocab_shard_bounds(int64_t V_total, int32_t num_shards, int32_t rank, int64_t* start, int64_t* len);
+
+/*
+ * Number of vocabulary splits of a V-column vocabulary (or shard): the row
+ * count of the split partial arrays part_m / part_s that
+ * grpo_head_logprob_shard writes and grpo_logprob_merge reads.  Returns 0 for
+ * V < 1.  Host only.
+ */
+int64_t gh_vocab_splits(int64_t V);
 
 /*
  * One rank's shard: head->W is the shard [head->V, D] holding global columns
  * [vocab_start, vocab_start + head->V) of V_total; targets are global ids.
  * Writes the shard's split partials part_m, part_s [S_shard, N] fp32
- * (S_shard = ceil(ceil(head->V / 256) / 4)) and zy [N] = z_{i, y_i} for the
- * rows whose target lies in the shard (other rows untouched).  vocab_start
- * must be a multiple of 1024 and every shard but the last whole splits.
+ * (S_shard = ceil(head->V / 256)) and zy [N] = z_{i, y_i} for the rows whose
+ * target lies in the shard (other rows untouched).  vocab_start must be a
+ * multiple of 256 and every shard but the last whole splits.
  */
 gh_status grpo_head_logprob_shard(const gh_head* head, int64_t vocab_start, int64_t V_total, float* part_m,
                                   float* part_s, float* zy, int32_t* status, void* stream);
@@ -309,7 +317,7 @@ gh_status grpo_group_advantage(const float* rewards, int32_t num_seqs, int32_t g
  * work overlaps in time, e.g. on two streams, race on it and must be
  * serialised by the caller.
  */
-#define GH_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define GH_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 gh_status grpo_head_forward_noalloc(const gh_head* head, const gh_grpo* grpo, float* logp, float* lse,
                                     float* coef, float* loss3, int32_t* status, void* stream);
 

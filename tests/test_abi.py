@@ -60,7 +60,7 @@ def test_struct_layout_matches_c(lib, tmp_path):
 
 
 def test_host_only_calls(lib):
-    assert lib.gh_abi_version() == 103
+    assert lib.gh_abi_version() == 104
     assert lib.gh_status_string(0) == b"GH_OK"
     assert lib.gh_status_string(3) == b"GH_ERR_WORKSPACE"
     assert lib.gh_kernel_kind_name(0) == b"fwd_logits_lse_tc"
@@ -75,10 +75,10 @@ def _head(N=1000, D=256, V=5000, dtype=0, row_tile=0, aligned=True):
 
 def test_workspace_sizes(lib):
     h = _head(N=1000, D=256, V=5000)
-    # forward: two [splits, N] fp32 partial arrays + zy [N]; splits = ceil(ceil(5000/256)/4) = 5
+    # forward: two [splits, N] fp32 partial arrays + zy [N]; splits = ceil(5000/256) = 20
     fw = lib.grpo_head_forward_workspace_size(ctypes.byref(h))
     al = lambda x: (x + 255) // 256 * 256
-    assert fw == 2 * al(5 * 1000 * 4) + al(1000 * 4)
+    assert fw == 2 * al(20 * 1000 * 4) + al(1000 * 4)
     # backward (bf16): one block of all 5120 padded columns, no dH accumulator
     bw = lib.grpo_head_backward_workspace_size(ctypes.byref(h))
     assert bw == al(1000 * 5120 * 2)
@@ -147,22 +147,24 @@ def test_binding_imports_without_gpu():
 
 def test_vocab_shard_bounds(lib):
     import gspo_logprob_gb300 as g
-    assert g.vocab_shard_bounds(5000, 2) == [(0, 3072), (3072, 1928)]
-    b = g.vocab_shard_bounds(151936, 4)   # 149 splits of 1024 -> 38, 37, 37, 37
-    assert b == [(0, 38912), (38912, 37888), (76800, 37888), (114688, 37248)]
+    assert [lib.gh_vocab_splits(v) for v in (0, 1, 256, 257, 5000, 151936)] == [0, 1, 1, 2, 20, 594]
+    assert g.vocab_shard_bounds(5000, 2) == [(0, 2560), (2560, 2440)]
+    b = g.vocab_shard_bounds(151936, 4)   # 594 splits of 256 -> 149, 149, 148, 148
+    assert b == [(0, 38144), (38144, 38144), (76288, 37888), (114176, 37760)]
     for V, P in ((5000, 5), (151936, 7), (1, 1), (1025, 2)):
         b = g.vocab_shard_bounds(V, P)
         assert b[0][0] == 0 and sum(x[1] for x in b) == V
-        assert all(x[0] % 1024 == 0 for x in b)
+        assert all(x[0] % 256 == 0 for x in b)
         assert all(b[i][0] + b[i][1] == b[i + 1][0] for i in range(P - 1))
     st, ln = ctypes.c_int64(), ctypes.c_int64()
-    assert lib.gh_vocab_shard_bounds(5000, 6, 0, ctypes.byref(st), ctypes.byref(ln)) == 1  # more shards than splits
+    assert lib.gh_vocab_shard_bounds(5000, 20, 0, ctypes.byref(st), ctypes.byref(ln)) == 0
+    assert lib.gh_vocab_shard_bounds(5000, 21, 0, ctypes.byref(st), ctypes.byref(ln)) == 1  # more shards than splits
 
 
 def test_shard_argument_validation(lib):
     h = _head(N=100, D=64, V=3000)
-    # vocab_start not on the 1024-column split grid
-    assert lib.grpo_head_logprob_shard(ctypes.byref(h), 512, 5000, 0x100, 0x100, 0x100, 0x100, None) == 1
+    # vocab_start not on the 256-column split grid
+    assert lib.grpo_head_logprob_shard(ctypes.byref(h), 384, 5000, 0x100, 0x100, 0x100, 0x100, None) == 1
     # a middle shard that is not whole splits
     assert lib.grpo_head_logprob_shard(ctypes.byref(h), 0, 5000, 0x100, 0x100, 0x100, 0x100, None) == 1
     assert b"whole" in lib.gh_last_error()

@@ -1,5 +1,5 @@
 """Vocabulary-parallel log-prob on one GPU: the vocabulary is cut into shards
-on the global 1024-column split grid, each shard runs as a separate call (as
+on the global 256-column split grid, each shard runs as a separate call (as
 a tensor-parallel rank would), the shard outputs are gathered in shard order
 and merged.  The result must equal the whole-vocabulary forward bit for bit,
 for every shard count; and match the fp64 oracle."""
@@ -36,7 +36,7 @@ def _tp_forward(H, W, y, m, V, P):
 @pytest.mark.parametrize("P", [2, 3, 5])
 def test_tp_equals_single_shard_bitwise(gpu_lib, dtype, P):
     import gspo_logprob_gb300 as g
-    w = make_workload(CONFIGS[1], dtype=dtype)   # N=4096, D=256, V=5000: 5 splits
+    w = make_workload(CONFIGS[1], dtype=dtype)   # N=4096, D=256, V=5000: 20 splits
     H, W, y, m = dev_head(w)
     base = g.grpo_head_forward(H, W, y, m)
     merged, st = _tp_forward(H, W, y, m, CONFIGS[1].V, P)
@@ -47,14 +47,14 @@ def test_tp_equals_single_shard_bitwise(gpu_lib, dtype, P):
 
 @pytest.mark.parametrize("P", [1, 4, 7])
 def test_tp_large_vocabulary_matches_oracle(gpu_lib, P):
-    # V = 20000 (20 splits, ragged last tile), N ragged, targets everywhere
+    # V = 20000 (79 splits, ragged last tile), N ragged, targets everywhere
     import gspo_logprob_gb300 as g
     rng = np.random.default_rng(P)
     N, D, V = 1000, 128, 20000
     Hf = rng.standard_normal((N, D), dtype=np.float32)
     Wf = (rng.standard_normal((V, D)) / math.sqrt(D)).astype(np.float32)
     y = rng.integers(0, V, N).astype(np.int32)
-    y[:5] = [0, 1023, 1024, V - 1, 19455]
+    y[:7] = [0, 255, 256, 1023, 1024, V - 1, 19967]
     w = dict(H=f32_to_bf16_bits(Hf), W=f32_to_bf16_bits(Wf), targets=y, mask=np.ones(N, np.uint8), dtype="bf16")
     Hd, Wd, yd, md = dev_head(w)
     merged, st = _tp_forward(Hd, Wd, yd, md, V, P)
