@@ -356,6 +356,7 @@ def run_ours(args, rank, world, local):
         "dlogits_tc": 2.0 * MB * N * D * V,
         "dh_gemm_tc": 2.0 * MB * N * D * V,
         "dw_gemm_tc": 2.0 * MB * N * D * V,
+        "dhdw_gemm_tc": 4.0 * MB * N * D * V,   # dH and dW of a block in one launch
     }
     kernels = {}
     for name, (n, tot) in prof.items():
@@ -524,6 +525,7 @@ def run_aux(args, rank, world, local):
     burst, _, hbm, src = measured_peaks()
     if dt == "bf16":
         alg = {k: 2.0 * N * D * V for k in ("fwd_logits_lse_tc", "dlogits_tc", "dh_gemm_tc", "dw_gemm_tc")}
+        alg["dhdw_gemm_tc"] = 4.0 * N * D * V
         bound, peak, peak_src = "tensor", burst, f"{src} bf16_tflops (burst: a short step timed alone)"
     else:
         alg = {"fwd_logits_lse_f32": 2.0 * N * D * V, "dlogits_f32": 2.0 * N * D * V, "gemm_f32": 4.0 * N * D * V}

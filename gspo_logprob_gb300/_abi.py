@@ -22,7 +22,7 @@ GH_BF16, GH_FP32 = 0, 1
 GH_TOKEN_MEAN, GH_SEQ_MEAN, GH_FIXED = 0, 1, 2
 REDUCTIONS = {"token_mean": GH_TOKEN_MEAN, "seq_mean": GH_SEQ_MEAN, "fixed": GH_FIXED}
 RATIO_LEVELS = {"token": 0, "sequence": 1}
-NUM_KERNEL_KINDS = 17
+NUM_KERNEL_KINDS = 18
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024  # GH_NOALLOC_SCRATCH_BYTES
 
 

@@ -211,6 +211,7 @@ static FwdWs fwd_layout(const gh_head* h, void* base) {
 struct BwdWs {
   void* G;
   float* acc32;
+  int* task_ctr;  // tile counter of the fused dH/dW launch
   int64_t vb;     // block width (columns)
   int64_t nblk;   // blocks
   size_t bytes;
@@ -227,7 +228,8 @@ static BwdWs bwd_layout(const gh_head* h, void* base) {
   char* b = static_cast<char*>(base);
   w.G = b;
   w.acc32 = acc ? reinterpret_cast<float*>(b + g) : nullptr;
-  w.bytes = g + acc;
+  w.task_ctr = reinterpret_cast<int*>(b + g + acc);
+  w.bytes = g + acc + 256;
   return w;
 }
 
@@ -553,11 +555,16 @@ static gh_status backward_impl(const gh_head* head, const float* lse, const floa
         mode = 1;
       }
       TcDhArgs ha{N, D, V, vb0, width, ldg, w.G, head->W, mode, acc32, dH, status};
-      e = run(K_DH_TC, st, [&] { return launch_dh_tc(ha, st); });
-      if (e != cudaSuccess) return cuda_fail(e, "dH launch");
       TcDwArgs wa{N, D, V, vb0, width, ldg, w.G, head->H, accumulate_dW, dW, status};
-      e = run(K_DW_TC, st, [&] { return launch_dw_tc(wa, st); });
-      if (e != cudaSuccess) return cuda_fail(e, "dW launch");
+      if (dhdw_fused()) {
+        e = run(K_DHDW_TC, st, [&] { return launch_dhdw_tc(ha, wa, w.task_ctr, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "dH/dW launch");
+      } else {
+        e = run(K_DH_TC, st, [&] { return launch_dh_tc(ha, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "dH launch");
+        e = run(K_DW_TC, st, [&] { return launch_dw_tc(wa, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "dW launch");
+      }
     } else {
       const float* H = static_cast<const float*>(head->H);
       const float* W = static_cast<const float*>(head->W);
@@ -665,7 +672,8 @@ const char* gh_kernel_kind_name(int32_t kind) {
   static const char* names[GH_NUM_KERNEL_KINDS] = {
       "fwd_logits_lse_tc", "merge_lse", "grpo_loss", "gspo_segment", "dlogits_tc", "dh_gemm_tc",
       "dw_gemm_tc", "group_advantage", "fwd_logits_lse_f32", "dlogits_f32", "gemm_f32", "timeout_probe",
-      "grpo_sequence_totals", "merge_lse_shards", "gspo_partials", "gspo_finish", "dh_merge"};
+      "grpo_sequence_totals", "merge_lse_shards", "gspo_partials", "gspo_finish", "dh_merge",
+      "dhdw_gemm_tc"};
   if (kind < 0 || kind >= GH_NUM_KERNEL_KINDS) return "";
   return names[kind];
 }

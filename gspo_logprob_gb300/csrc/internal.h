@@ -44,6 +44,7 @@ enum KernelKind {
   K_GSPO_PARTIALS = 14,
   K_GSPO_FINISH = 15,
   K_DH_MERGE = 16,
+  K_DHDW_TC = 17,
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -107,6 +108,11 @@ struct TcDwArgs {  // dW[vb0:vb0+width] (+)= G[:, :width]^T H
   int* status;
 };
 cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st);
+// dH and dW of one vocabulary block in one launch of CTA pairs with tiles
+// handed out from *task_ctr (a device int the call zeroes first).  Used when
+// dhdw_fused() (the CTA-pair kernels are on and GH_BWD_FUSED is not 0).
+bool dhdw_fused();
+cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, cudaStream_t st);
 
 // --- fp32 SIMT launchers (simt_kernels.cu) ----------------------------------
 struct F32FwdArgs {

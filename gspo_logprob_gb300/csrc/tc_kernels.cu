@@ -5,6 +5,7 @@
 #include "internal.h"
 #include "tc_gemm.cuh"
 #include "tc_gemm_pair.cuh"
+#include "tc_gemm_dual.cuh"
 
 namespace gh {
 
@@ -105,6 +106,13 @@ int dh_pair() {
 }
 int dw_pair() {
   static const int v = pair_knob("GH_DW_PAIR", 1);
+  return v;
+}
+
+// dH and dW of a block in one launch with dynamically handed-out tiles (1,
+// default) or as two launches (0); only with both pair knobs on
+int bwd_fused_knob() {
+  static const int v = pair_knob("GH_BWD_FUSED", 1);
   return v;
 }
 
@@ -299,6 +307,100 @@ cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st) {
   TcSched sc = make_sched(static_cast<int>(ceil_div(rows, 2 * TC_BM)), nn, 1, nkb, 2 * TC_BM, dw_group_m());
   if (dw_cg() == 2) return launch_tc<2, 2, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
   return launch_tc<2, 1, true, true, EpiStore>(ta, tb, sc, 0, 0, ep, a.status, st);
+}
+
+bool dhdw_fused() { return bwd_fused_knob() == 1 && dh_pair() == 1 && dw_pair() == 1; }
+
+cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, cudaStream_t st) {
+  // dH: A = G [N, ldg] K-major, B = W [V, D] MN-major (rows vb0.. of the block)
+  CUtensorMap ta_h, tb_h, ta_w, tb_w;
+  if (!make_tmap_bf16(&ta_h, h.G, h.ldg, h.N, static_cast<uint64_t>(h.ldg) * 2, TC_BK, TC_BM))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb_h, h.W, h.D, h.V, static_cast<uint64_t>(h.D) * 2, 64, TC_BK)) return cudaErrorInvalidValue;
+  // dW: A = G^T (G read MN-major), B = H [N, D] MN-major
+  if (!make_tmap_bf16(&ta_w, w.G, w.ldg, w.N, static_cast<uint64_t>(w.ldg) * 2, 64, TC_BK))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb_w, w.H, w.D, w.N, static_cast<uint64_t>(w.D) * 2, 64, TC_BK)) return cudaErrorInvalidValue;
+  EpiStore::Params eh;
+  eh.M_valid = h.N;
+  eh.N_valid = h.D;
+  eh.row_off = 0;
+  eh.ld = h.D;
+  eh.mode = h.mode;
+  eh.out32 = h.acc32;
+  eh.out16 = static_cast<__nv_bfloat16*>(h.out16);
+  const int rows = w.V - w.vb0 < w.width ? w.V - w.vb0 : w.width;
+  EpiStore::Params ew;
+  ew.M_valid = rows;
+  ew.N_valid = w.D;
+  ew.row_off = w.vb0;
+  ew.ld = w.D;
+  ew.mode = w.accumulate ? 1 : 0;
+  ew.out32 = w.dW;
+  ew.out16 = nullptr;
+  PairJob jh, jw;
+  jh.sc = make_sched(static_cast<int>(ceil_div(h.N, 2 * TC_BM)), static_cast<int>(ceil_div(h.D, TC_BN)), 1,
+                     static_cast<int>(ceil_div(h.width, TC_BK)), 2 * TC_BM, dh_group_m());
+  jh.b_off_n = 0;
+  jh.b_off_k = h.vb0;
+  jh.a_mn = 0;
+  jh.b_mn = 1;
+  jw.sc = make_sched(static_cast<int>(ceil_div(rows, 2 * TC_BM)), static_cast<int>(ceil_div(w.D, TC_BN)), 1,
+                     static_cast<int>(ceil_div(w.N, TC_BK)), 2 * TC_BM, dw_group_m());
+  jw.b_off_n = 0;
+  jw.b_off_k = 0;
+  jw.a_mn = 1;
+  jw.b_mn = 1;
+  const int tasks = jh.sc.num_tasks + jw.sc.num_tasks;
+  if (tasks <= 0) return cudaSuccess;
+
+  using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PairJob, PairJob, EpiStore::Params,
+                        EpiStore::Params, int*, int*, uint64_t);
+  Kern kern = tc_dual_pair_kernel<EpiStore>;
+  static bool attr_set = false;
+  static int pairs_fit = 0;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DUAL_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(2 * max_pairs());
+    q.blockDim = dim3(TcPairCfg::THREADS);
+    q.dynamicSmemBytes = DUAL_SMEM_BYTES;
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = 2;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    q.attrs = qa;
+    q.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) n = max_pairs();
+    pairs_fit = n < max_pairs() ? n : max_pairs();
+    attr_set = true;
+  }
+  cudaError_t e = cudaMemsetAsync(task_ctr, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  const int pairs = tasks < pairs_fit ? tasks : pairs_fit;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(TcPairCfg::THREADS);
+  cfg.dynamicSmemBytes = DUAL_SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // the product with the deeper K (longer tiles) first: the short tiles of
+  // the other fill the end of the list
+  if (jw.sc.num_kb > jh.sc.num_kb)
+    e = cudaLaunchKernelEx(&cfg, kern, ta_w, tb_w, ta_h, tb_h, jw, jh, ew, eh, task_ctr, h.status, timeout_ns());
+  else
+    e = cudaLaunchKernelEx(&cfg, kern, ta_h, tb_h, ta_w, tb_w, jh, jw, eh, ew, task_ctr, h.status, timeout_ns());
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace gh

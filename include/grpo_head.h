@@ -337,9 +337,10 @@ int32_t gh_abi_version(void);
  * Kinds: 0 fwd logits+LSE, 1 merge, 2 GRPO loss, 3 GSPO loss, 4 dlogits,
  * 5 dH GEMM, 6 dW GEMM, 7 advantage, 8 fp32 forward, 9 fp32 dlogits,
  * 10 fp32 GEMM, 11 timeout probe, 12 GRPO loss from sequence totals, 13 shard merge,
- * 14 GSPO partials, 15 GSPO loss from partials, 16 dH shard merge.
+ * 14 GSPO partials, 15 GSPO loss from partials, 16 dH shard merge, 17 dH and dW
+ * GEMMs of a vocabulary block in one launch.
  */
-#define GH_NUM_KERNEL_KINDS 17
+#define GH_NUM_KERNEL_KINDS 18
 void gh_profile_enable(int32_t on);
 void gh_profile_reset(void);
 gh_status gh_profile_read(int32_t kind, int64_t* launches, double* total_ms);

@@ -81,13 +81,13 @@ def test_workspace_sizes(lib):
     assert fw == 2 * al(20 * 1000 * 4) + al(1000 * 4)
     # backward (bf16): one block of all 5120 padded columns, no dH accumulator
     bw = lib.grpo_head_backward_workspace_size(ctypes.byref(h))
-    assert bw == al(1000 * 5120 * 2)
+    assert bw == al(1000 * 5120 * 2) + 256          # + the tile counter of the fused dH/dW launch
     # a vocabulary of two 16384-column blocks adds the fp32 dH accumulator
     h3 = _head(N=1000, D=256, V=20000)
-    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h3)) == al(1000 * 16384 * 2) + al(1000 * 256 * 4)
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h3)) == al(1000 * 16384 * 2) + al(1000 * 256 * 4) + 256
     # a single-block vocabulary needs no accumulator
     h2 = _head(N=64, D=64, V=500)
-    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h2)) == al(64 * 512 * 2)
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h2)) == al(64 * 512 * 2) + 256
     # invalid problem -> 0
     assert lib.grpo_head_forward_workspace_size(ctypes.byref(_head(D=12))) == 0
 

@@ -27,6 +27,7 @@ SETTINGS = [
     {"GH_FWD_PAIR": "1", "GH_DLOGITS_PAIR": "1", "GH_DH_PAIR": "1", "GH_DW_PAIR": "1", "GH_BWD_BLOCK_COLS": "1024"},
     {"GH_FWD_PAIR": "0", "GH_DLOGITS_PAIR": "0", "GH_DH_PAIR": "0", "GH_DW_PAIR": "0"},
     {"GH_FWD_PAIR": "0", "GH_DLOGITS_PAIR": "1", "GH_DH_PAIR": "0", "GH_DW_PAIR": "1", "GH_BWD_BLOCK_COLS": "768"},
+    {"GH_BWD_FUSED": "0", "GH_BWD_BLOCK_COLS": "512"},            # dH and dW as two pair launches per block
 ]
 
 
@@ -39,3 +40,27 @@ def test_tuning_settings_match_oracle(gpu_lib, env, dtype):
                        text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("ok")
+
+
+def _child(env, dtype="bf16"):
+    full = dict(os.environ)
+    full.update(env)
+    r = subprocess.run([sys.executable, os.path.join(HERE, "knob_child.py"), dtype], env=full, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    words = r.stdout.split()
+    return dict(x.split("=", 1) for x in words if "=" in x)
+
+
+def test_backward_bits_do_not_depend_on_kernel_variant(gpu_lib):
+    # a tile is always one chain of MMAs over K in the same order, whichever
+    # kernel computes it: the fused dH/dW launch with dynamically handed-out
+    # tiles, two pair launches, or the single-CTA kernels give the same bits
+    # for the same vocabulary block width
+    base = _child({"GH_BWD_BLOCK_COLS": "512"})
+    unfused = _child({"GH_BWD_BLOCK_COLS": "512", "GH_BWD_FUSED": "0"})
+    single = _child({"GH_BWD_BLOCK_COLS": "512", "GH_DLOGITS_PAIR": "0", "GH_DH_PAIR": "0", "GH_DW_PAIR": "0"})
+    assert base == unfused == single, (base, unfused, single)
+    # dW does not depend on the block width either (each element's K runs over the tokens)
+    wide = _child({"GH_BWD_BLOCK_COLS": "1024"})
+    assert wide["dW"] == base["dW"]
