@@ -59,12 +59,14 @@ int dlogits_group_m() {
   static const int v = kind_group_m("GH_DLOGITS_GROUP_M", 16);
   return v;
 }
+// dH / dW: groups of 8 row tiles (a 76-tile wave then touches the fewest
+// distinct operand bytes; measured +0.7% over 16 on the fused launch)
 int dh_group_m() {
-  static const int v = kind_group_m("GH_DH_GROUP_M", 16);
+  static const int v = kind_group_m("GH_DH_GROUP_M", 8);
   return v;
 }
 int dw_group_m() {
-  static const int v = kind_group_m("GH_DW_GROUP_M", 16);
+  static const int v = kind_group_m("GH_DW_GROUP_M", 8);
   return v;
 }
 
