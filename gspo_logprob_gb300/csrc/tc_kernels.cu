@@ -1,6 +1,7 @@
 // tcgen05 kernels of the bf16 path: logits + online LSE (forward), dlogits
 // recompute (backward) and the dH / dW GEMMs, all instances of tc_gemm_kernel.
 #include <cstdlib>
+#include <mutex>
 
 #include "internal.h"
 #include "tc_gemm.cuh"
@@ -70,17 +71,62 @@ int dw_group_m() {
   return v;
 }
 
+// Launch set-up of one kernel instance, done once per device under a lock:
+// the dynamic shared-memory limit is a per-device function attribute, and the
+// number of CTA pairs that fit is queried after it is set.
+struct KernSetup {
+  std::mutex mu;
+  bool done[64] = {};
+  int pairs[64] = {};
+};
+
+int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev < 0 || dev >= 64 ? 0 : dev;
+}
+
+// sets the shared-memory attribute; with `cluster_pairs` also returns how many
+// 2-CTA clusters of `threads` threads fit on the device (at most max_pairs())
+int max_pairs();
+cudaError_t kern_setup(KernSetup& s, const void* kern, int smem, int threads, bool cluster_pairs, int* pairs) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> g(s.mu);
+  if (!s.done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    if (cluster_pairs) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(2 * max_pairs());
+      q.blockDim = dim3(threads);
+      q.dynamicSmemBytes = smem;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 2;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) n = max_pairs();
+      (void)cudaGetLastError();
+      if (n > max_pairs()) n = max_pairs();
+    }
+    s.pairs[dev] = n;
+    s.done[dev] = true;
+  }
+  if (pairs) *pairs = s.pairs[dev];
+  return cudaSuccess;
+}
+
 template <int MT, int CG, bool A_MN, bool B_MN, class Epi>
 cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const TcSched& sc, int b_off_n, int b_off_k,
                       const typename Epi::Params& ep, int* status, cudaStream_t st) {
   using C = TcCfg<MT, CG>;
   auto kern = tc_gemm_kernel<MT, CG, A_MN, B_MN, Epi>;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static KernSetup setup;  // per instantiation
+  cudaError_t e = kern_setup(setup, reinterpret_cast<const void*>(kern), C::SMEM_BYTES, C::THREADS, false, nullptr);
+  if (e != cudaSuccess) return e;
   if (sc.num_tasks <= 0) return cudaSuccess;
   const int grid = static_cast<int>(sc.num_tasks < num_sms() ? sc.num_tasks : num_sms());
   kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, sc, b_off_n, b_off_k, ep, status, timeout_ns());
@@ -132,27 +178,10 @@ cudaError_t launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const T
                            const typename Epi::Params& ep, int* status, cudaStream_t st) {
   using C = TcPairCfg;
   auto kern = tc_gemm_pair_kernel<A_MN, B_MN, Epi>;
-  static bool attr_set = false;  // per instantiation
-  static int pairs_fit = 0;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t q = {};
-    q.gridDim = dim3(2 * max_pairs());
-    q.blockDim = dim3(C::THREADS);
-    q.dynamicSmemBytes = C::SMEM_BYTES;
-    cudaLaunchAttribute qa[1];
-    qa[0].id = cudaLaunchAttributeClusterDimension;
-    qa[0].val.clusterDim.x = 2;
-    qa[0].val.clusterDim.y = 1;
-    qa[0].val.clusterDim.z = 1;
-    q.attrs = qa;
-    q.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) n = max_pairs();
-    pairs_fit = n < max_pairs() ? n : max_pairs();
-    attr_set = true;
-  }
+  static KernSetup setup;  // per instantiation
+  int pairs_fit = 0;
+  cudaError_t e0 = kern_setup(setup, reinterpret_cast<const void*>(kern), C::SMEM_BYTES, C::THREADS, true, &pairs_fit);
+  if (e0 != cudaSuccess) return e0;
   if (sc.num_tasks <= 0) return cudaSuccess;
   const int pairs = sc.num_tasks < pairs_fit ? sc.num_tasks : pairs_fit;
   cudaLaunchConfig_t cfg = {};
@@ -359,28 +388,12 @@ cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, 
   using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PairJob, PairJob, EpiStore::Params,
                         EpiStore::Params, int*, int*, uint64_t);
   Kern kern = tc_dual_pair_kernel<EpiStore>;
-  static bool attr_set = false;
-  static int pairs_fit = 0;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DUAL_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t q = {};
-    q.gridDim = dim3(2 * max_pairs());
-    q.blockDim = dim3(TcPairCfg::THREADS);
-    q.dynamicSmemBytes = DUAL_SMEM_BYTES;
-    cudaLaunchAttribute qa[1];
-    qa[0].id = cudaLaunchAttributeClusterDimension;
-    qa[0].val.clusterDim.x = 2;
-    qa[0].val.clusterDim.y = 1;
-    qa[0].val.clusterDim.z = 1;
-    q.attrs = qa;
-    q.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) n = max_pairs();
-    pairs_fit = n < max_pairs() ? n : max_pairs();
-    attr_set = true;
-  }
-  cudaError_t e = cudaMemsetAsync(task_ctr, 0, sizeof(int), st);
+  static KernSetup setup;
+  int pairs_fit = 0;
+  cudaError_t e = kern_setup(setup, reinterpret_cast<const void*>(kern), DUAL_SMEM_BYTES, TcPairCfg::THREADS, true,
+                             &pairs_fit);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(task_ctr, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
   const int pairs = tasks < pairs_fit ? tasks : pairs_fit;
   cudaLaunchConfig_t cfg = {};
