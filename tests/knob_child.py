@@ -63,7 +63,7 @@ def main(dtype):
         assert torch.equal(o2["logp"].view(torch.int32), ref["logp"].view(torch.int32)), rt
     import hashlib
     dig = lambda t: hashlib.sha256(t.contiguous().cpu().view(torch.uint8).numpy().tobytes()).hexdigest()[:16]
-    print("ok", dtype, e, "dW=" + dig(bw["dW"]), "dH=" + dig(bw["dH"]))
+    print("ok", dtype, e, "dW=" + dig(bw["dW"]), "dH=" + dig(bw["dH"]), "lse=" + dig(fw["lse"]), "logp=" + dig(fw["logp"]))
 
 
 if __name__ == "__main__":

@@ -64,3 +64,12 @@ def test_backward_bits_do_not_depend_on_kernel_variant(gpu_lib):
     # dW does not depend on the block width either (each element's K runs over the tokens)
     wide = _child({"GH_BWD_BLOCK_COLS": "1024"})
     assert wide["dW"] == base["dW"]
+
+
+def test_forward_bits_do_not_depend_on_raster(gpu_lib):
+    # the forward's raster group only changes which tiles run together; every
+    # tile's partial and the fixed-order merge are the same
+    base = _child({})
+    for g in ("1", "3", "0"):
+        other = _child({"GH_FWD_GROUP_M": g})
+        assert (other["lse"], other["logp"]) == (base["lse"], base["logp"]), g
