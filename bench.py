@@ -328,8 +328,9 @@ def run_ours(args, rank, world, local):
 
     # ---- end to end: pinned host inputs -> device, step, losses -> host.  A user
     # overlaps the upload of micro-batch k+1 (copy stream) with the compute of
-    # micro-batch k (two input slots); every byte still crosses inside the timed
-    # region, and the step ends with the losses read back on the host.
+    # micro-batch k (two input slots), and the next step's first upload with this
+    # step's last micro-batch; every byte still crosses inside the timed region,
+    # and each step ends with its losses read back on the host.
     e2e = None
     if not args.no_e2e:
         hosts = (Hh, yh, mh, sh, rh, oldh, refh)
@@ -352,23 +353,33 @@ def run_ours(args, rank, world, local):
                     b.copy_(hx[k], non_blocking=True)
                 copied[s].record(copy_stream)
 
-        def e2e_step():
-            upload(0)
+        def e2e_step(first_uploaded, prefetch_next):
+            # micro-batch k uses slot k % 2 (MB is even, so the next step's
+            # micro-batch 0 goes to slot 0 while this step's last one uses slot 1)
+            if not first_uploaded:
+                upload(0)
             for k in range(MB):
                 if k + 1 < MB:
                     upload(k + 1)
+                elif prefetch_next:
+                    upload(0)
                 comp.wait_event(copied[k % 2])
                 micro_step(k, *slots[k % 2])
                 freed[k % 2].record(comp)
             loss_h.copy_(loss3, non_blocking=True)
             torch.cuda.synchronize()
 
-        for it in range(args.warmup + args.steps):
+        total = args.warmup + args.steps
+        prefetched = False
+        for it in range(total):
             if it == args.warmup:
                 barrier(world)
                 torch.cuda.synchronize()
                 t0 = time.perf_counter()
-            e2e_step()
+            # the timed region's first upload is its own; the last step prefetches nothing
+            nxt = MB % 2 == 0 and it + 1 < total and it + 1 != args.warmup
+            e2e_step(prefetched, nxt)
+            prefetched = nxt
         wall = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
         ops.raise_on_status(status)
         e2e = {"value": world * MB * N / wall, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
