@@ -70,6 +70,14 @@ class _Workspace:
 WORKSPACE = _Workspace()
 
 
+def _caller_workspace(ws: torch.Tensor, nbytes: int) -> torch.Tensor:
+    if not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if ws.numel() * ws.element_size() < nbytes:
+        raise ValueError(f"workspace holds {ws.numel() * ws.element_size()} bytes; the call needs {nbytes}")
+    return ws
+
+
 def make_head(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor, mask: torch.Tensor,
               row_tile: int = 0) -> GhHead:
     _need(H, "H")
@@ -110,12 +118,19 @@ def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=
                       num_seqs: int = 0, eps_low: float = 0.2, eps_high: float = 0.2, beta: float = 0.0,
                       reduction: str = "token_mean", norm: float = 0.0, delta: float = 0.0,
                       ratio_level: str = "token", seq_totals: bool = False, row_tile: int = 0,
-                      want_coef: bool = True, status: Optional[torch.Tensor] = None, out: Optional[dict] = None):
+                      want_coef: bool = True, status: Optional[torch.Tensor] = None, out: Optional[dict] = None,
+                      workspace: Optional[torch.Tensor] = None):
     """Selected-token log-probs and LSE; with ``old_logp`` given, also the GRPO
     loss (loss, policy_loss, kl) and coef = d loss / d logp.  ``delta`` > 0
     caps the unclipped ratio (two-sided clip); ``ratio_level="sequence"`` uses
     one ratio per sequence; ``seq_totals`` also returns the per-sequence totals
     (seq_policy, seq_kl, seq_count) for a data-parallel reduction.
+
+    ``workspace``: a caller-owned CUDA byte buffer of at least
+    forward_workspace_bytes(head) bytes; by default the binding's shared,
+    grow-only buffer is used.  A call captured into a CUDA graph keeps the
+    workspace address it was given, so pass your own buffer when capturing
+    (the shared one may be replaced by a larger one later).
 
     Returns a dict with logp, lse, and (GRPO) coef, loss3, plus status."""
     head = make_head(H, W, targets, mask, row_tile)
@@ -150,7 +165,7 @@ def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=
             coef = out.get("coef") if out.get("coef") is not None else torch.empty(N, dtype=_F32, device=dev)
         loss3 = out.get("loss3") if out.get("loss3") is not None else torch.empty(3, dtype=_F32, device=dev)
     nbytes = forward_workspace_bytes(head)
-    ws = WORKSPACE.get(dev, nbytes)
+    ws = _caller_workspace(workspace, nbytes) if workspace is not None else WORKSPACE.get(dev, nbytes)
     code = _lib().grpo_head_forward(ctypes.byref(head), ctypes.byref(g) if g is not None else None, _ptr(logp),
                                     _ptr(lse), _ptr(coef), _ptr(loss3), _ptr(st), _ptr(ws), nbytes, _stream(dev))
     _abi.check(code, "grpo_head_forward")
@@ -350,8 +365,11 @@ def gspo_segment_loss_from_partials(logp, mask, seg_id, num_segments: int, fsum_
 
 
 def grpo_head_backward(H, W, targets, mask, lse, coef, *, grad_out=None, dH=None, dW=None,
-                       accumulate_dW: bool = False, row_tile: int = 0, status: Optional[torch.Tensor] = None):
-    """dH [N, D] (dtype of H) and dW [V, D] fp32 from each row's LSE and coef."""
+                       accumulate_dW: bool = False, row_tile: int = 0, status: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None):
+    """dH [N, D] (dtype of H) and dW [V, D] fp32 from each row's LSE and coef.
+    ``workspace`` as in grpo_head_forward, at least backward_workspace_bytes(head)
+    bytes."""
     head = make_head(H, W, targets, mask, row_tile)
     dev = H.device
     N, D, V = head.N, head.D, head.V
@@ -371,7 +389,7 @@ def grpo_head_backward(H, W, targets, mask, lse, coef, *, grad_out=None, dH=None
         _need(dW, "dW", _F32, (V, D))
     st = new_status(dev) if status is None else status
     nbytes = backward_workspace_bytes(head)
-    ws = WORKSPACE.get(dev, nbytes)
+    ws = _caller_workspace(workspace, nbytes) if workspace is not None else WORKSPACE.get(dev, nbytes)
     code = _lib().grpo_head_backward(ctypes.byref(head), _ptr(lse), _ptr(coef), _ptr(grad_out), _ptr(dH), _ptr(dW),
                                      1 if accumulate_dW else 0, _ptr(st), _ptr(ws), nbytes, _stream(dev))
     _abi.check(code, "grpo_head_backward")
