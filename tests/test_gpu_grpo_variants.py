@@ -1,7 +1,8 @@
 """GPU parity of the GRPO variants against the fp64 oracle: the two-sided
 clip cap (delta), one importance ratio per sequence, and the deterministic
 data-parallel reduction (per-sequence totals gathered in sequence order give
-the single-call loss bit for bit)."""
+the single-call loss bit for bit; advantage groups cut across ranks; dW
+partials summed in rank order)."""
 import numpy as np
 import pytest
 import torch
@@ -119,3 +120,51 @@ def test_data_parallel_split_is_bitwise_identical(gpu_lib, reduction, ratio_leve
     for sl, r in parts:
         assert torch.equal(r["coef"].view(torch.int32), whole["coef"][sl].view(torch.int32))
         assert torch.equal(r["logp"].view(torch.int32), whole["logp"][sl].view(torch.int32))
+
+
+def test_data_parallel_straddling_group_and_rank_ordered_dW(gpu_lib):
+    # two "ranks" own whole sequences of one batch, cut inside an advantage
+    # group (8 sequences, G = 8, cut after 3).  Each rank normalises advantages
+    # from the gathered rewards of all sequences, runs forward + backward on its
+    # tokens with the global normaliser and a fresh dW, and the dW partials are
+    # summed in rank order.  That sum is bitwise the single-process accumulation
+    # over the same two pieces (dW of piece 0 stored, piece 1 added), each
+    # rank's dH rows are bitwise the whole-batch dH rows, and dW matches the
+    # oracle over the whole batch.
+    import gspo_logprob_gb300 as g
+    cfg, w, H, W = _prepare(0.05)    # ratios inside the clip band: no gradient switches at its edges
+    Hd, Wd, y, m = dev_head(w)
+    S, G = w["num_seqs"], w["group_size"]
+    seq = w["seq_id"]
+    rew = dev_tensor(w["rewards"])
+    adv_all = g.grpo_group_advantage(rew, G)
+    norm = float(w["mask"].sum())
+    common = dict(eps_low=cfg.eps_low, eps_high=cfg.eps_high, beta=cfg.beta, norm=norm)
+    whole_fw = g.grpo_head_forward(Hd, Wd, y, m, old_logp=dev_tensor(w["old"]), ref_logp=dev_tensor(w["ref"]),
+                                   adv=adv_all, seq_id=dev_tensor(seq), num_seqs=S, **common)
+    whole_bw = g.grpo_head_backward(Hd, Wd, y, m, whole_fw["lse"], whole_fw["coef"])
+    pieces = []
+    for s0, s1 in ((0, 3), (3, S)):
+        t0, t1 = int(np.searchsorted(seq, s0, "left")), int(np.searchsorted(seq, s1, "left"))
+        sl = slice(t0, t1)
+        gathered = torch.cat([rew[:s0], rew[s0:s1], rew[s1:]])      # all-gather of the per-rank rewards
+        adv = g.grpo_group_advantage(gathered, G)[s0:s1].contiguous()
+        assert torch.equal(adv.view(torch.int32), adv_all[s0:s1].view(torch.int32))
+        args = (Hd[sl].contiguous(), Wd, y[sl].contiguous(), m[sl].contiguous())
+        fw = g.grpo_head_forward(*args, old_logp=dev_tensor(w["old"][sl]), ref_logp=dev_tensor(w["ref"][sl]),
+                                 adv=adv, seq_id=dev_tensor(seq[sl] - s0), num_seqs=s1 - s0, **common)
+        bw = g.grpo_head_backward(*args, fw["lse"], fw["coef"])
+        pieces.append((sl, args, fw, bw))
+    reduced = g.grpo_dh_merge(torch.stack([p[3]["dW"] for p in pieces]), dtype=torch.float32)
+    # the same pieces accumulated in one process
+    acc = None
+    for k, (sl, args, fw, _) in enumerate(pieces):
+        acc = g.grpo_head_backward(*args, fw["lse"], fw["coef"], dW=acc, accumulate_dW=k > 0)["dW"]
+    torch.cuda.synchronize()
+    assert torch.equal(reduced.view(torch.int32), acc.view(torch.int32))
+    for sl, _, _, bw in pieces:
+        assert torch.equal(bw["dH"].view(torch.int16), whole_bw["dH"][sl].view(torch.int16))
+    o = oracle.forward_backward(H, W, w["targets"], w["mask"], seq, w["adv"].astype(np.float64), S,
+                                w["old"].astype(np.float64), w["ref"].astype(np.float64), cfg.eps_low, cfg.eps_high,
+                                cfg.beta, norm=norm)
+    assert_grad_bf16(reduced.cpu().numpy(), o["dW"], "dW reduced over ranks")
