@@ -45,6 +45,7 @@ AUX_WORKLOADS = {
     "selective_logp_bf16": (1, "bf16", "fwd"),
     "selective_logp_f32": (1, "fp32", "fwd"),
     "grpo_small_f32": (2, "fp32", "fwd+grpo+bwd"),
+    "tiny_fp32_grpo": (0, "fp32", "fwd+grpo+bwd"),
 }
 # fp32 FMA peak of the SIMT twin: 152 SMs x 128 fp32 lanes x 2 FLOP x 2070 MHz
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
@@ -624,6 +625,10 @@ def run_aux(args, rank, world, local):
                    "l2": "flushed between timed steps (512 MB write outside the events)"},
         "tflops": round(flops_step / (ms_step * 1e-3) / 1e12, 2), "roofline": roof, "kernels": kernels,
         "gpu_launches": launches, "clocks": clk, "e2e": None,
+        "peak_extra_mem": {"workspace_bytes": max(ws_f.numel(), ws_b.numel() if what != "fwd" else 0),
+                           "NxVx2_bytes": N * V * 2,
+                           "workspace_frac": round(max(ws_f.numel(), ws_b.numel() if what != "fwd" else 0)
+                                                   / (N * V * 2), 4)},
     }
     if "gspo_segment" in kernels:
         nbytes = N * (4 + 4 + 1 + 4 + 4) + 8 * w["num_seqs"]
@@ -632,7 +637,7 @@ def run_aux(args, rank, world, local):
                             "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1), "hbm_peak_GB_per_s": hbm,
                             "bound": "latency (one launch over %d KB)" % (nbytes // 1024)}
     if not args.no_cpu_baseline:
-        rows = {1: N, 2: N, 3: 256}[idx]
+        rows = {0: N, 1: N, 2: N, 3: 256}[idx]
         tps, secs, cores, desc = oracle_sample_aux(cfg, w, dt, what, rows)
         res["cpu_baseline"] = {"value": round(tps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                "sample": desc, "seconds": round(secs, 2)}
