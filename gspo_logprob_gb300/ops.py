@@ -50,7 +50,8 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
 
 
 class _Workspace:
-    """Grow-only scratch buffer per device (reused across calls)."""
+    """Grow-only scratch buffer per device, reused by consecutive calls (not
+    safe for calls that overlap on different streams)."""
 
     def __init__(self):
         self._buf = {}
@@ -128,9 +129,11 @@ def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=
 
     ``workspace``: a caller-owned CUDA byte buffer of at least
     forward_workspace_bytes(head) bytes; by default the binding's shared,
-    grow-only buffer is used.  A call captured into a CUDA graph keeps the
-    workspace address it was given, so pass your own buffer when capturing
-    (the shared one may be replaced by a larger one later).
+    grow-only buffer is used.  The shared buffer serves one stream at a time:
+    calls whose GPU work overlaps on different streams must each pass their
+    own.  A call captured into a CUDA graph keeps the workspace address it was
+    given, so pass your own buffer when capturing (the shared one may be
+    replaced by a larger one later).
 
     Returns a dict with logp, lse, and (GRPO) coef, loss3, plus status."""
     head = make_head(H, W, targets, mask, row_tile)
