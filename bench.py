@@ -61,8 +61,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--micro-batches", type=int, default=None, help="override (testing only)")
-    ap.add_argument("--cpu-rows", type=int, default=384,
-                    help="tokens in the oracle's timed sample (about 10-20 s of host work on 16 cores)")
+    ap.add_argument("--cpu-rows", type=int, default=768,
+                    help="tokens in the oracle's timed sample (about 12 s of host work on 16 Arm cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
