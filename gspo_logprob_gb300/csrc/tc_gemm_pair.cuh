@@ -25,7 +25,7 @@ struct TcPairCfg {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;        // 16 KB: this CTA's 128 rows
   static constexpr int B_BYTES = (TC_BN / 2) * TC_BK * 2;  // 16 KB: this CTA's 128 columns
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 6;
+  static constexpr int STAGES = 7;  // 224 KB: the deepest pipeline that fits
   static constexpr int EPI_WARPS = 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
