@@ -34,7 +34,8 @@
  *    `int32_t *status` (GH_DEV_* bits) without a host synchronisation; the
  *    caller reads it when it chooses.  `status` must be zeroed by the caller.
  *  - Row-major layouts; 16-byte aligned base pointers; bf16 rows need
- *    D % 8 == 0, fp32 rows D % 4 == 0.
+ *    D % 8 == 0 (16-byte TMA row pitch); fp32 rows take any D (vector loads
+ *    when D % 4 == 0, scalar loads otherwise).
  *  - Results are deterministic (no floating-point atomics) and logp/LSE are
  *    bitwise independent of row_tile and of the other rows in the batch.
  */
