@@ -335,6 +335,9 @@ int32_t gh_abi_version(void);
  * counted per kernel kind; gh_profile_read returns, for kind k, the launch
  * count and the summed event time (ms) since the last reset (it synchronises
  * the recorded events).  gh_launch_count counts all launches since load.
+ * The instrumentation state is process-wide and unsynchronised: enable it only
+ * while a single host thread calls the library, and not during a CUDA-graph
+ * capture.
  * Kinds: 0 fwd logits+LSE, 1 merge, 2 GRPO loss, 3 GSPO loss, 4 dlogits,
  * 5 dH GEMM, 6 dW GEMM, 7 advantage, 8 fp32 forward, 9 fp32 dlogits,
  * 10 fp32 GEMM, 11 timeout probe, 12 GRPO loss from sequence totals, 13 shard merge,
