@@ -139,6 +139,8 @@ static cudaEvent_t pool_event() {
   return e;
 }
 
+void count_extra_launch() { ++g_prof.launches_total; }
+
 template <class F>
 static cudaError_t run(int kind, cudaStream_t st, F&& f) {
   ++g_prof.launches_total;
@@ -212,6 +214,8 @@ struct BwdWs {
   void* G;
   float* acc32;
   int* task_ctr;  // tile counter of the fused dH/dW launch
+  float* splitk;  // fp32 path: split-K partial products of the dH / dW GEMMs
+  int ks_dh, ks_dw;
   int64_t vb;     // block width (columns)
   int64_t nblk;   // blocks
   size_t bytes;
@@ -225,11 +229,22 @@ static BwdWs bwd_layout(const gh_head* h, void* base) {
   const size_t elt = h->dtype == GH_BF16 ? 2 : 4;
   const size_t g = align_up(static_cast<size_t>(h->N) * w.vb * elt, 256);
   const size_t acc = (h->dtype == GH_BF16 && w.nblk > 1) ? align_up(static_cast<size_t>(h->N) * h->D * 4, 256) : 0;
+  // fp32: dH is [N, D] over K = block width, dW is [block width, D] over K = N
+  w.ks_dh = w.ks_dw = 1;
+  size_t sk = 0;
+  if (h->dtype != GH_BF16) {
+    w.ks_dh = gemm_f32_ksplit(h->N, h->D, w.vb);
+    w.ks_dw = gemm_f32_ksplit(w.vb, h->D, h->N);
+    const size_t a1 = w.ks_dh > 1 ? static_cast<size_t>(w.ks_dh) * h->N * h->D * 4 : 0;
+    const size_t a2 = w.ks_dw > 1 ? static_cast<size_t>(w.ks_dw) * w.vb * h->D * 4 : 0;
+    sk = align_up(a1 > a2 ? a1 : a2, 256);
+  }
   char* b = static_cast<char*>(base);
   w.G = b;
   w.acc32 = acc ? reinterpret_cast<float*>(b + g) : nullptr;
   w.task_ctr = reinterpret_cast<int*>(b + g + acc);
-  w.bytes = g + acc + 256;
+  w.splitk = sk ? reinterpret_cast<float*>(b + g + acc + 256) : nullptr;
+  w.bytes = g + acc + 256 + sk;
   return w;
 }
 
@@ -574,12 +589,16 @@ static gh_status backward_impl(const gh_head* head, const float* lse, const floa
       if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
       const int real = static_cast<int>((V - vb0) < width ? (V - vb0) : width);
       // dH[N, D] (+)= G[:, :real] W[vb0:vb0+real, :]
+      // the last block may be narrower than the widths the split was sized for: fewer slices then
+      const int ks_h = w.ks_dh > 1 ? gemm_f32_ksplit(N, D, real) : 1;
       F32GemmArgs ha{N, D, real, G, ldg, 1, W + static_cast<size_t>(vb0) * D, D, 1, static_cast<float*>(dH), D, 0,
-                     b > 0 ? 1 : 0};
+                     b > 0 ? 1 : 0, ks_h < w.ks_dh ? ks_h : w.ks_dh, w.splitk};
       e = run(K_GEMM_F32, st, [&] { return launch_gemm_f32(ha, st); });
       if (e != cudaSuccess) return cuda_fail(e, "dH launch");
       // dW[vb0 + v, :] (+)= sum_i G[i, v] H[i, :]
-      F32GemmArgs wa{real, D, N, G, 1, ldg, H, D, 1, dW, D, vb0, accumulate_dW ? 1 : 0};
+      const int ks_w = w.ks_dw > 1 ? gemm_f32_ksplit(real, D, N) : 1;
+      F32GemmArgs wa{real, D, N, G, 1, ldg, H, D, 1, dW, D, vb0, accumulate_dW ? 1 : 0,
+                     ks_w < w.ks_dw ? ks_w : w.ks_dw, w.splitk};
       e = run(K_GEMM_F32, st, [&] { return launch_gemm_f32(wa, st); });
       if (e != cudaSuccess) return cuda_fail(e, "dW launch");
     }

@@ -151,8 +151,18 @@ struct F32GemmArgs {
   long long ldc;
   int row_off;
   int accumulate;
+  // split K (small output grids): ksplit slices write partial [ksplit, M, Nn]
+  // products to `scratch`, then one kernel adds them to C in slice order
+  int ksplit;
+  float* scratch;
 };
 cudaError_t launch_gemm_f32(const F32GemmArgs& a, cudaStream_t st);
+// K slices for an fp32 GEMM of this shape (a function of the shape only, so the
+// bits do not depend on the GPU) and the scratch they need
+int gemm_f32_ksplit(long long M, long long Nn, long long K);
+// one more kernel launched inside a counted call (gh_launch_count)
+void count_extra_launch();
+constexpr size_t F32_SPLITK_SCRATCH_MAX = size_t(64) << 20;
 
 // --- loss kernels (loss_kernels.cu) -----------------------------------------
 cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const float* part_s, const float* zy,

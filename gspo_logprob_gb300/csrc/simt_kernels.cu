@@ -238,25 +238,25 @@ __global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
   float4 pa[2], pb[2];
   // A chunk: 128 x 16.  k-contiguous: element e = t + 256q -> row e/4, k 4(e%4).
   // m-contiguous: e -> k e/32, rows 4(e%32)..
-  auto fetch = [&](int k0) {
+  auto fetch = [&](int k0, int k_end) {
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int e = t + 256 * q;
       if (A_KCONTIG) {
         const int m = e >> 2, kq = (e & 3) * 4;
         const int gm = m0 + m;
-        pa[q] = gm < a.M ? load4<VEC>(a.A + static_cast<long long>(gm) * a.sam, k0 + kq, a.K)
+        pa[q] = gm < a.M ? load4<VEC>(a.A + static_cast<long long>(gm) * a.sam, k0 + kq, k_end)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
       } else {
         const int k = e >> 5, mq = (e & 31) * 4;
         const int gk = k0 + k;
-        pa[q] = gk < a.K ? load4<VEC>(a.A + static_cast<long long>(gk) * a.sak, m0 + mq, a.M)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        pa[q] = gk < k_end ? load4<VEC>(a.A + static_cast<long long>(gk) * a.sak, m0 + mq, a.M)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       const int k = e >> 5, nq = (e & 31) * 4;
       const int gk = k0 + k;
-      pb[q] = gk < a.K ? load4<VEC>(a.B + static_cast<long long>(gk) * a.sbk, n0 + nq, a.Nn)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      pb[q] = gk < k_end ? load4<VEC>(a.B + static_cast<long long>(gk) * a.sbk, n0 + nq, a.Nn)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
   auto stash = [&](int buf) {
@@ -278,13 +278,17 @@ __global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
     }
   };
 
-  const int nk = (a.K + G_BK - 1) / G_BK;
-  fetch(0);
+  // K range of this slice (blockIdx.z) in G_BK steps; loads past k_end read 0
+  const int kslice = ((a.K + a.ksplit - 1) / a.ksplit + G_BK - 1) / G_BK * G_BK;
+  const int k_beg = blockIdx.z * kslice;
+  const int k_end = min(a.K, k_beg + kslice);
+  const int nk = k_end > k_beg ? (k_end - k_beg + G_BK - 1) / G_BK : 0;
+  fetch(k_beg, k_end);
   stash(0);
   __syncthreads();
   for (int kc = 0; kc < nk; ++kc) {
     const int buf = kc & 1;
-    if (kc + 1 < nk) fetch((kc + 1) * G_BK);
+    if (kc + 1 < nk) fetch(k_beg + (kc + 1) * G_BK, k_end);
 #pragma unroll
     for (int k = 0; k < G_BK; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * tr]);
@@ -303,17 +307,32 @@ __global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
       __syncthreads();
     }
   }
+  const bool partial = a.ksplit > 1;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int gm = m0 + (i < 4 ? 4 * tr : 64 + 4 * tr) + (i & 3);
     if (gm >= a.M) continue;
-    float* crow = a.C + (static_cast<long long>(a.row_off) + gm) * a.ldc;
+    float* crow = partial ? a.scratch + (static_cast<long long>(blockIdx.z) * a.M + gm) * a.Nn
+                          : a.C + (static_cast<long long>(a.row_off) + gm) * a.ldc;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int gn = n0 + (j < 4 ? 4 * tc : 64 + 4 * tc) + (j & 3);
       if (gn >= a.Nn) continue;
-      crow[gn] = a.accumulate ? (crow[gn] + acc[i][j]) : acc[i][j];
+      crow[gn] = (!partial && a.accumulate) ? (crow[gn] + acc[i][j]) : acc[i][j];
     }
+  }
+}
+
+// C[row_off + m, n] = (accumulate ? C : 0) + sum over slices z = 0, 1, ... of scratch[z, m, n]
+__global__ void __launch_bounds__(256) f32_splitk_reduce_kernel(F32GemmArgs a) {
+  const long long total = static_cast<long long>(a.M) * a.Nn;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long m = i / a.Nn, n = i % a.Nn;
+    float* c = a.C + (a.row_off + m) * a.ldc + n;
+    float v = a.accumulate ? *c : 0.f;
+    for (int z = 0; z < a.ksplit; ++z) v += a.scratch[z * total + i];
+    *c = v;
   }
 }
 
@@ -349,10 +368,24 @@ cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+int gemm_f32_ksplit(long long M, long long Nn, long long K) {
+  // aim for at least 256 CTAs of 128 x 128 outputs, slices of at least 512 in K,
+  // at most 8 slices, scratch within F32_SPLITK_SCRATCH_MAX
+  const long long tiles = ceil_div(M, G_BM) * ceil_div(Nn, G_BN);
+  if (tiles <= 0 || tiles >= 256 || K < 1024) return 1;
+  long long s = ceil_div(256, tiles);
+  s = s < 8 ? s : 8;
+  s = s < K / 512 ? s : K / 512;
+  while (s > 1 && static_cast<size_t>(s * M * Nn) * 4 > F32_SPLITK_SCRATCH_MAX) --s;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
 cudaError_t launch_gemm_f32(const F32GemmArgs& a, cudaStream_t st) {
   if (a.M <= 0 || a.Nn <= 0) return cudaSuccess;
   if (a.sbn != 1 || (a.sak != 1 && a.sam != 1)) return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>(ceil_div(a.Nn, G_BN)), static_cast<unsigned>(ceil_div(a.M, G_BM)));
+  if (a.ksplit < 1 || (a.ksplit > 1 && !a.scratch)) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>(ceil_div(a.Nn, G_BN)), static_cast<unsigned>(ceil_div(a.M, G_BM)),
+            static_cast<unsigned>(a.ksplit));
   const bool kc = a.sak == 1;
   const long long lda = kc ? a.sam : a.sak;
   const bool vec = aligned16(a.A) && aligned16(a.B) && lda % 4 == 0 && a.sbk % 4 == 0;
@@ -366,6 +399,14 @@ cudaError_t launch_gemm_f32(const F32GemmArgs& a, cudaStream_t st) {
       f32_gemm_kernel<false, true><<<grid, 256, 0, st>>>(a);
     else
       f32_gemm_kernel<false, false><<<grid, 256, 0, st>>>(a);
+  }
+  if (a.ksplit > 1) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long total = static_cast<long long>(a.M) * a.Nn;
+    const unsigned blocks = static_cast<unsigned>(ceil_div(total, 256) < 4096 ? ceil_div(total, 256) : 4096);
+    f32_splitk_reduce_kernel<<<blocks, 256, 0, st>>>(a);
+    count_extra_launch();
   }
   return cudaGetLastError();
 }
