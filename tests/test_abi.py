@@ -88,6 +88,14 @@ def test_workspace_sizes(lib):
     # a single-block vocabulary needs no accumulator
     h2 = _head(N=64, D=64, V=500)
     assert lib.grpo_head_backward_workspace_size(ctypes.byref(h2)) == al(64 * 512 * 2) + 256
+    # fp32, N = D = 1024, V = 4096: the G block [1024, 4096] fp32, the counter, and the
+    # split-K scratch of dH (8 x 8 output tiles < 256 -> 4 slices of K = 4096: 4 x 1024 x 1024
+    # fp32); dW ([4096, 1024] = 256 tiles) is not split
+    h4 = _head(N=1024, D=1024, V=4096, dtype=1)
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h4)) == al(1024 * 4096 * 4) + 256 + al(4 * 1024 * 1024 * 4)
+    # a large fp32 problem needs no split
+    h5 = _head(N=8192, D=4096, V=4096, dtype=1)
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h5)) == al(8192 * 4096 * 4) + 256
     # invalid problem -> 0
     assert lib.grpo_head_forward_workspace_size(ctypes.byref(_head(D=12))) == 0
 
