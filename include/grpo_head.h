@@ -27,7 +27,9 @@
  *    from the fixed scratch array of grpo_head_forward_noalloc (scratch space is
  *    otherwise the caller's `ws` buffer, sized by the *_workspace_size calls).
  *  - All work is enqueued asynchronously on `stream` (a cudaStream_t passed as
- *    void*; NULL = the legacy default stream).  Nothing synchronises.
+ *    void*; NULL = the legacy default stream).  Nothing synchronises.  The work
+ *    is kernels and asynchronous memsets only, so calls can be captured into a
+ *    CUDA graph; a captured call keeps the `ws` address it was given.
  *  - The return value reports argument and launch errors (gh_status); a
  *    message for the last error of the calling thread is in gh_last_error().
  *  - Data-dependent problems are OR-ed into the caller's device word
@@ -83,8 +85,10 @@ typedef struct {
   int64_t V;              /* real vocabulary size; padding to 256 columns is internal     */
   int32_t dtype;          /* gh_dtype of H, W and dH: bf16 (fp32 accumulate, tensor
                              cores) or fp32 (exact fp32 FMA, no TF32)                    */
-  int32_t row_tile;       /* 0 = default (128) | 64 | 128 | 256: rows per work unit; the
-                             results do not depend on it (bitwise)                       */
+  int32_t row_tile;       /* 0 = default | 64 | 128 | 256: rows per work unit (bf16: 64
+                             and 128 run single-CTA tiles, 256 and the default CTA-pair
+                             tiles; fp32: rows per CTA, default 64); the results do not
+                             depend on it (bitwise)                                      */
   const void* H;          /* [N, D] row-major                                            */
   const void* W;          /* [V, D] row-major                                            */
   const int32_t* targets; /* [N] selected token ids y_i                                  */
