@@ -28,9 +28,9 @@
  *    otherwise the caller's `ws` buffer, sized by the *_workspace_size calls).
  *  - All work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *    void*; NULL = the legacy default stream).  Nothing synchronises.  The work
- *    is kernels and asynchronous memsets only, so the calls that take a `ws`
- *    buffer can be captured into a CUDA graph; a captured call keeps the `ws`
- *    address it was given.
+ *    is kernels and asynchronous memsets only, so these calls can be captured
+ *    into a CUDA graph (a captured call keeps the `ws` address it was given);
+ *    grpo_head_forward_noalloc is described on its own below.
  *  - The return value reports argument and launch errors (gh_status); a
  *    message for the last error of the calling thread is in gh_last_error().
  *  - Data-dependent problems are OR-ed into the caller's device word
