@@ -195,6 +195,29 @@ def measured_peaks():
 _ORACLE_CACHE = {}
 
 
+def o_n_bytes(name: str, N: int, splits: int, with_ref: bool):
+    """Algorithmic HBM bytes of one launch of an O(N) kernel over N tokens: every
+    input read once, every output written once (None for other kernels)."""
+    if name == "merge_lse":        # part_m, part_s [splits, N]; zy, targets, mask -> logp, lse
+        return 8 * splits * N + 17 * N
+    if name == "grpo_loss":        # logp, old, ref, mask, seq_id -> coef
+        return 21 * N
+    if name == "gspo_segment":     # logp, old (, ref), mask, seg_id -> coef
+        return (21 if with_ref else 17) * N
+    return None
+
+
+def add_o_n_rates(kernels: dict, N: int, splits: int, with_ref: bool, hbm: float):
+    for name, ent in kernels.items():
+        nb = o_n_bytes(name, N, splits, with_ref)
+        if nb is None:
+            continue
+        sec = ent.get("avg_launch_ms", ent.get("avg_launch_us", 0) * 1e-3) * 1e-3
+        ent["algorithmic_bytes"] = nb
+        ent["gb_per_s"] = round(nb / sec / 1e9, 1) if sec > 0 else None
+        ent["hbm_frac"] = round(nb / sec / 1e9 / hbm, 4) if sec > 0 and hbm > 0 else None
+
+
 def oracle_sample(cfg, rows: int, norm: float):
     """Time the fp64 oracle on `rows` tokens of micro-batch 0 (full V and D):
     logits + LSE, GRPO loss terms and the dH / dW contributions of those rows.
@@ -281,15 +304,16 @@ def run_ours(args, rank, world, local):
     dH = torch.empty(MB, N, D, dtype=torch.bfloat16, device=dev)
     dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     loss3 = torch.empty(MB, 3, dtype=torch.float32, device=dev)
+    clipped = torch.zeros(MB, dtype=torch.int32, device=dev)
     outs = [dict(logp=torch.empty(N, device=dev), lse=torch.empty(N, device=dev), coef=torch.empty(N, device=dev),
-                 loss3=loss3[k]) for k in range(MB)]
+                 loss3=loss3[k], num_clipped=clipped[k:k + 1]) for k in range(MB)]
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def micro_step(k, Hk, yk, mk, seqk, rewk, oldk, refk):
         adv = g.grpo_group_advantage(rewk, G, status=status)
         fw = g.grpo_head_forward(Hk, W, yk, mk, old_logp=oldk, ref_logp=refk, adv=adv, seq_id=seqk, num_seqs=nseq,
                                  eps_low=cfg.eps_low, eps_high=cfg.eps_high, beta=cfg.beta, norm=norm,
-                                 status=status, out=outs[k])
+                                 clip_count=True, status=status, out=outs[k])
         g.grpo_head_backward(Hk, W, yk, mk, fw["lse"], fw["coef"], dH=dH[k], dW=dW, accumulate_dW=k > 0,
                              status=status)
 
@@ -410,6 +434,7 @@ def run_ours(args, rank, world, local):
         if name in alg:
             ent["tflops"] = round(alg[name] / (per_step_ms * 1e-3) / 1e12, 1)
         kernels[name] = ent
+    add_o_n_rates(kernels, N, -(-V // 256), True, hbm)
     dom = max((k for k in kernels if k in alg), key=lambda k: kernels[k]["ms_per_step"])
     dom_launches = kernels[dom]["launches_per_step"]
     roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["tflops"], "peak": sustained,
@@ -439,6 +464,9 @@ def run_ours(args, rank, world, local):
                            "measured_frac": round(peak_mem / (N * V * 2), 4)},
         "clocks": clk,
         "e2e": e2e,
+        "clip_fraction": {"clipped_tokens": int(clipped.sum().item()), "active_tokens": int(norm),
+                          "value": round(int(clipped.sum().item()) / max(norm, 1.0), 6),
+                          "what": "active tokens of the last step whose policy gradient the clip cuts off"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, secs, cores, desc = oracle_sample(cfg, args.cpu_rows, norm)
@@ -522,6 +550,7 @@ def run_aux(args, rank, world, local):
         dW = torch.empty(V, D, dtype=torch.float32, device=dev)
         out.update(coef=torch.empty(N, device=dev), loss3=torch.empty(3, device=dev))
 
+    last = {}  # the last step's clipped count (device tensor)
     head = ops.make_head(H, W, y, m)
     ws_f = torch.empty(ops.forward_workspace_bytes(head), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(ops.backward_workspace_bytes(head), dtype=torch.uint8, device=dev)
@@ -533,13 +562,16 @@ def run_aux(args, rank, world, local):
         adv = g.grpo_group_advantage(rew, G, status=status)
         if cfg.kind == "gspo":
             fw = g.grpo_head_forward(H, W, y, m, status=status, out=out, workspace=ws_f)
-            coef = g.gspo_segment_loss(fw["logp"], old, m, seq, S, adv, eps_low=cfg.eps_low, eps_high=cfg.eps_high,
-                                       divisor=float(S), status=status)["coef"]
+            gs = g.gspo_segment_loss(fw["logp"], old, m, seq, S, adv, eps_low=cfg.eps_low, eps_high=cfg.eps_high,
+                                     divisor=float(S), status=status)
+            coef = gs["coef"]
+            last["clipped"] = gs["num_clipped"]
         else:
             fw = g.grpo_head_forward(H, W, y, m, old_logp=old, ref_logp=ref, adv=adv, seq_id=seq, num_seqs=S,
                                      eps_low=cfg.eps_low, eps_high=cfg.eps_high, beta=cfg.beta, status=status,
-                                     out=out, workspace=ws_f)
+                                     out=out, workspace=ws_f, clip_count=True)
             coef = fw["coef"]
+            last["clipped"] = fw["num_clipped"]
         g.grpo_head_backward(H, W, y, m, fw["lse"], coef, dH=dH, dW=dW, status=status, workspace=ws_b)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -605,6 +637,7 @@ def run_aux(args, rank, world, local):
         if name in alg:
             ent["tflops"] = round(alg[name] / (per_step_ms * 1e-3) / 1e12, 2)
         kernels[name] = ent
+    add_o_n_rates(kernels, N, -(-V // 256), cfg.kind != "gspo", hbm)
     if kernels:
         dom = max((k for k in kernels if k in alg), key=lambda k: kernels[k]["ms_per_step"])
         roof = {"kernel": dom, "bound": bound, "achieved": kernels[dom]["tflops"], "peak": round(peak, 1),
@@ -630,12 +663,17 @@ def run_aux(args, rank, world, local):
                            "workspace_frac": round(max(ws_f.numel(), ws_b.numel() if what != "fwd" else 0)
                                                    / (N * V * 2), 4)},
     }
-    if "gspo_segment" in kernels:
-        nbytes = N * (4 + 4 + 1 + 4 + 4) + 8 * w["num_seqs"]
-        us = kernels["gspo_segment"]["avg_launch_us"]
-        res["gspo_seam"] = {"us_per_launch": us, "algorithmic_bytes": nbytes,
-                            "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1), "hbm_peak_GB_per_s": hbm,
-                            "bound": "latency (one launch over %d KB)" % (nbytes // 1024)}
+    if "clipped" in last:
+        nclip = int(last["clipped"].item())
+        if cfg.kind == "gspo":
+            live = int(np.sum(np.bincount(w["seq_id"][(w["seq_id"] >= 0) & (w["mask"] > 0)],
+                                          minlength=w["num_seqs"]) > 0))
+            res["clip_fraction"] = {"clipped": nclip, "of": live, "value": round(nclip / max(live, 1), 4),
+                                    "what": "live segments whose policy gradient the clip cuts off"}
+        else:
+            act = int(w["mask"].sum())
+            res["clip_fraction"] = {"clipped": nclip, "of": act, "value": round(nclip / max(act, 1), 6),
+                                    "what": "active tokens whose policy gradient the clip cuts off"}
     if not args.no_cpu_baseline:
         rows = {0: N, 1: N, 2: N, 3: 256}[idx]
         tps, secs, cores, desc = oracle_sample_aux(cfg, w, dt, what, rows)

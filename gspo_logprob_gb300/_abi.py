@@ -35,24 +35,27 @@ class GhGrpo(ctypes.Structure):
     _fields_ = [("old_logp", c_void_p), ("ref_logp", c_void_p), ("adv", c_void_p), ("seq_id", c_void_p),
                 ("num_seqs", c_int32), ("reduction", c_int32), ("eps_low", c_float), ("eps_high", c_float),
                 ("beta", c_float), ("delta", c_float), ("norm", c_double), ("ratio_level", c_int32),
-                ("reserved", c_int32), ("seq_policy", c_void_p), ("seq_kl", c_void_p), ("seq_count", c_void_p)]
+                ("reserved", c_int32), ("seq_policy", c_void_p), ("seq_kl", c_void_p), ("seq_count", c_void_p),
+                ("num_clipped", c_void_p)]
 
 
 # name -> (restype, argtypes)
 SIGNATURES = {
     "grpo_head_forward_workspace_size": (c_size_t, [POINTER(GhHead)]),
     "grpo_head_backward_workspace_size": (c_size_t, [POINTER(GhHead)]),
+    "grpo_head_backward_shard_workspace_size": (c_size_t, [POINTER(GhHead), c_int64]),
     "grpo_head_forward": (c_int32, [POINTER(GhHead), POINTER(GhGrpo), c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_size_t, c_void_p]),
+    "gspo_segment_workspace_size": (c_size_t, [c_int32]),
     "gspo_segment_loss": (c_int32, [c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p,
                                     c_float, c_float, c_float, c_double, c_int32, c_void_p, c_void_p, c_void_p,
-                                    c_void_p, c_void_p, c_void_p]),
+                                    c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "gspo_segment_partials": (c_int32, [c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
-                                        c_void_p, c_void_p, c_void_p, c_void_p]),
+                                        c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "gspo_segment_loss_from_partials": (c_int32, [c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
                                                   c_void_p, c_void_p, c_void_p, c_float, c_float, c_float, c_double,
                                                   c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                                  c_void_p]),
+                                                  c_void_p, c_void_p, c_size_t, c_void_p]),
     "grpo_head_backward": (c_int32, [POINTER(GhHead), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                      c_void_p, c_void_p, c_size_t, c_void_p]),
     "grpo_group_advantage": (c_int32, [c_void_p, c_int32, c_int32, c_float, c_void_p, c_void_p, c_void_p]),

@@ -195,6 +195,7 @@ struct FwdWs {
   float* part_m;
   float* part_s;
   float* zy;
+  void* loss;  // per-sequence slots of the GRPO loss
   size_t bytes;
 };
 static FwdWs fwd_layout(const gh_head* h, void* base) {
@@ -206,44 +207,100 @@ static FwdWs fwd_layout(const gh_head* h, void* base) {
   w.part_m = reinterpret_cast<float*>(b);
   w.part_s = reinterpret_cast<float*>(b + a);
   w.zy = reinterpret_cast<float*>(b + 2 * a);
-  w.bytes = 2 * a + z;
+  w.loss = b + 2 * a + z;
+  w.bytes = 2 * a + z + grpo_loss_scratch_bytes(N);
   return w;
+}
+
+// Backward plan.  The vocabulary is walked in blocks of vb columns (the bf16
+// dlogits block G [rows, vb] lives in the workspace) and the rows in chunks of
+// nc tokens, each chunk finishing its dH over all blocks before the next one
+// starts and adding its dW contribution to dW.  nc keeps the workspace within
+// three quarters of N * V * 2 bytes (the bf16 [N, V] logits the method never
+// forms): one chunk of all N rows unless the vocabulary is narrow next to the
+// block and accumulator rows.  nc depends on N, D, dtype and the WHOLE
+// vocabulary only (V_total, also for a vocabulary shard), so that every
+// vocabulary shard adds dW over the same row chunks as the single-shard call
+// and its dW rows come out bitwise equal.  dH rows never depend on nc.
+constexpr double BWD_MEM_FRACTION = 0.75;
+
+// Vocabulary block width: bf16 16384 columns (GH_BWD_BLOCK_COLS), fp32 at most
+// 1024 (the fp32 dlogits block is twice as wide in bytes, and narrow blocks
+// keep whole-batch row chunks on small problems); never wider than the padded
+// vocabulary.
+static int64_t vocab_block(int64_t V, int dtype) {
+  const int64_t Vp = ceil_div(V, VTILE) * VTILE;
+  int64_t cols = bwd_block_cols();
+  if (dtype != GH_BF16 && cols > 1024) cols = 1024;
+  return Vp < cols ? Vp : cols;
+}
+
+static double bwd_budget(int64_t N, int64_t V) {
+  return BWD_MEM_FRACTION * 2.0 * static_cast<double>(N) * static_cast<double>(V);
+}
+
+static int64_t bwd_rows_per_chunk(int64_t N, int64_t D, int64_t V_total, int dtype) {
+  const bool bf16 = dtype == GH_BF16;
+  const int64_t vb = vocab_block(V_total, dtype);
+  const int64_t nblk = ceil_div(ceil_div(V_total, VTILE) * VTILE, vb);
+  const double per_row = static_cast<double>(vb) * (bf16 ? 2 : 4) + ((bf16 && nblk > 1) ? 4.0 * D : 0.0);
+  const double budget = bwd_budget(N, V_total);
+  const int64_t gran = bf16 ? 128 : 64;  // one row tile of the single-CTA tensor-core / fp32 kernels
+  if (N <= gran || static_cast<double>(N) * per_row <= budget) return N;
+  // the most rows that fit, in whole row tiles (at least one), then spread
+  // evenly over the chunks that takes
+  int64_t nc_max = static_cast<int64_t>(budget / per_row) / gran * gran;
+  if (nc_max < gran) nc_max = gran;
+  const int64_t nch = ceil_div(N, nc_max);
+  int64_t nc = ceil_div(ceil_div(N, nch), gran) * gran;
+  if (nc > nc_max) nc = nc_max;
+  return nc < N ? nc : N;
 }
 
 struct BwdWs {
   void* G;
   float* acc32;
   int* task_ctr;  // tile counter of the fused dH/dW launch
-  float* splitk;  // fp32 path: split-K partial products of the dH / dW GEMMs
-  int ks_dh, ks_dw;
+  float* slices;  // fp32 path: partials of the K slices that run in parallel
+  size_t slice_bytes;
   int64_t vb;     // block width (columns)
   int64_t nblk;   // blocks
+  int64_t nc;     // rows per chunk
+  int64_t nch;    // chunks
   size_t bytes;
 };
-static BwdWs bwd_layout(const gh_head* h, void* base) {
+// dh_partial: a vocabulary shard's backward, whose fp32 dH partial is the
+// caller's output (no accumulator needed)
+static BwdWs bwd_layout(const gh_head* h, void* base, int64_t V_total, bool dh_partial) {
   const int64_t Vp = ceil_div(h->V, VTILE) * VTILE;
   BwdWs w;
-  const int64_t cols = bwd_block_cols();
-  w.vb = Vp < cols ? Vp : cols;
+  w.vb = vocab_block(h->V, h->dtype);
   w.nblk = ceil_div(Vp, w.vb);
-  const size_t elt = h->dtype == GH_BF16 ? 2 : 4;
-  const size_t g = align_up(static_cast<size_t>(h->N) * w.vb * elt, 256);
-  const size_t acc = (h->dtype == GH_BF16 && w.nblk > 1) ? align_up(static_cast<size_t>(h->N) * h->D * 4, 256) : 0;
-  // fp32: dH is [N, D] over K = block width, dW is [block width, D] over K = N
-  w.ks_dh = w.ks_dw = 1;
+  w.nc = bwd_rows_per_chunk(h->N, h->D, V_total, h->dtype);
+  w.nch = w.nc > 0 ? ceil_div(h->N, w.nc) : 0;
+  const bool bf16 = h->dtype == GH_BF16;
+  const size_t g = align_up(static_cast<size_t>(w.nc) * w.vb * (bf16 ? 2 : 4), 256);
+  const size_t acc = (bf16 && w.nblk > 1 && !dh_partial) ? align_up(static_cast<size_t>(w.nc) * h->D * 4, 256) : 0;
+  // fp32: scratch for the K slices of the dH / dW GEMMs that run in parallel,
+  // as much as their output grids can use within what the budget leaves (at
+  // most 64 MB; none means every GEMM runs its slices inside each CTA)
   size_t sk = 0;
-  if (h->dtype != GH_BF16) {
-    w.ks_dh = gemm_f32_ksplit(h->N, h->D, w.vb);
-    w.ks_dw = gemm_f32_ksplit(w.vb, h->D, h->N);
-    const size_t a1 = w.ks_dh > 1 ? static_cast<size_t>(w.ks_dh) * h->N * h->D * 4 : 0;
-    const size_t a2 = w.ks_dw > 1 ? static_cast<size_t>(w.ks_dw) * w.vb * h->D * 4 : 0;
-    sk = align_up(a1 > a2 ? a1 : a2, 256);
+  if (!bf16) {
+    const double left = bwd_budget(h->N, h->V) - static_cast<double>(g + acc + 256);
+    size_t room = left > 0 ? static_cast<size_t>(left) / 256 * 256 : 0;
+    if (room > (size_t(64) << 20)) room = size_t(64) << 20;
+    const int p_dh = gemm_f32_par(w.nc, h->D, w.vb, room);
+    const int p_dw = gemm_f32_par(w.vb, h->D, w.nc, room);
+    const size_t s_dh = p_dh > 1 ? static_cast<size_t>(p_dh) * w.nc * h->D * 4 : 0;
+    const size_t s_dw = p_dw > 1 ? static_cast<size_t>(p_dw) * w.vb * h->D * 4 : 0;
+    sk = align_up(s_dh > s_dw ? s_dh : s_dw, 256);
   }
   char* b = static_cast<char*>(base);
   w.G = b;
   w.acc32 = acc ? reinterpret_cast<float*>(b + g) : nullptr;
   w.task_ctr = reinterpret_cast<int*>(b + g + acc);
-  w.splitk = sk ? reinterpret_cast<float*>(b + g + acc + 256) : nullptr;
+  w.slices = sk ? reinterpret_cast<float*>(b + g + acc + 256) : nullptr;
+  w.slice_bytes = sk;
   w.bytes = g + acc + 256 + sk;
   return w;
 }
@@ -254,7 +311,7 @@ using namespace gh;
 
 extern "C" {
 
-int32_t gh_abi_version(void) { return 104; }
+int32_t gh_abi_version(void) { return 106; }
 
 const char* gh_status_string(gh_status s) {
   switch (s) {
@@ -276,7 +333,13 @@ size_t grpo_head_forward_workspace_size(const gh_head* head) {
 
 size_t grpo_head_backward_workspace_size(const gh_head* head) {
   if (check_head(head) != GH_OK) return 0;
-  return bwd_layout(head, nullptr).bytes;
+  return bwd_layout(head, nullptr, head->V, false).bytes;
+}
+
+size_t grpo_head_backward_shard_workspace_size(const gh_head* head, int64_t V_total) {
+  if (check_head(head) != GH_OK) return 0;
+  if (V_total < head->V || V_total > (int64_t(1) << 28)) return 0;
+  return bwd_layout(head, nullptr, V_total, true).bytes;
 }
 
 gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* logp, float* lse, float* coef,
@@ -330,7 +393,9 @@ gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* log
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   if (grpo) {
-    cudaError_t e = run(K_GRPO, st, [&] { return launch_grpo(N, logp, head->mask, grpo, coef, loss3, status, st); });
+    void* scratch = (ws && N > 0) ? fwd_layout(head, ws).loss : nullptr;
+    cudaError_t e =
+        run(K_GRPO, st, [&] { return launch_grpo(N, logp, head->mask, grpo, coef, loss3, status, scratch, st); });
     if (e != cudaSuccess) return cuda_fail(e, "GRPO loss launch");
   }
   return GH_OK;
@@ -462,39 +527,58 @@ static gh_status check_gspo_loss_args(const float* ref_logp, float beta, const f
   return GH_OK;
 }
 
+size_t gspo_segment_workspace_size(int32_t num_segments) {
+  if (num_segments < 1 || num_segments > MAX_SEQS) return 0;
+  return gspo_scratch_bytes(num_segments);
+}
+
+// ws of a seam call: NULL (one CTA) or at least gspo_segment_workspace_size bytes
+static gh_status check_gspo_ws(int32_t num_segments, void* ws, size_t ws_bytes) {
+  if (ws && ws_bytes < gspo_scratch_bytes(num_segments))
+    return fail(GH_ERR_WORKSPACE, "GSPO workspace needs %zu bytes, got %zu", gspo_scratch_bytes(num_segments),
+                ws_bytes);
+  if (ws && !aligned16(ws)) return fail(GH_ERR_INVALID_ARG, "GSPO workspace must be 16-byte aligned");
+  return GH_OK;
+}
+
 gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp, const float* ref_logp,
                             const uint8_t* mask, const int32_t* seg_id, int32_t num_segments, const float* seg_adv,
                             float eps_low, float eps_high, float beta, double divisor, int32_t token_weighted,
-                            float* loss, float* seg_ratio, float* coef, float* mean_logp, int32_t* status,
-                            void* stream) {
+                            float* loss, float* seg_ratio, float* coef, float* mean_logp, int32_t* num_clipped,
+                            int32_t* status, void* ws, size_t ws_bytes, void* stream) {
   g_last_error.clear();
   gh_status s = check_gspo_common(N, logp, mask, seg_id, num_segments, status);
   if (s != GH_OK) return s;
   if (N > 0 && !old_logp) return fail(GH_ERR_INVALID_ARG, "old_logp is NULL");
   s = check_gspo_loss_args(ref_logp, beta, seg_adv, eps_low, eps_high, divisor, loss, coef, N);
   if (s != GH_OK) return s;
+  s = check_gspo_ws(num_segments, ws, ws_bytes);
+  if (s != GH_OK) return s;
   if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   GspoArgs g{static_cast<int>(N), logp, old_logp, beta != 0.f ? ref_logp : nullptr, mask, seg_id, num_segments,
-             seg_adv, eps_low, eps_high, beta, divisor, token_weighted, loss, seg_ratio, coef, mean_logp, status};
-  cudaError_t e = run(K_GSPO, st, [&] { return launch_gspo(g, st); });
+             seg_adv, eps_low, eps_high, beta, divisor, token_weighted, loss, seg_ratio, coef, mean_logp,
+             num_clipped, status};
+  cudaError_t e = run(K_GSPO, st, [&] { return launch_gspo(g, ws, st); });
   if (e != cudaSuccess) return cuda_fail(e, "GSPO launch");
   return GH_OK;
 }
 
 gh_status gspo_segment_partials(int64_t N, const float* logp, const float* old_logp, const float* ref_logp,
                                 const uint8_t* mask, const int32_t* seg_id, int32_t num_segments, float* fsum,
-                                int32_t* cnt, int32_t* status, void* stream) {
+                                int32_t* cnt, int32_t* status, void* ws, size_t ws_bytes, void* stream) {
   g_last_error.clear();
   gh_status s = check_gspo_common(N, logp, mask, seg_id, num_segments, status);
   if (s != GH_OK) return s;
   if (N > 0 && !old_logp) return fail(GH_ERR_INVALID_ARG, "old_logp is NULL");
   if (!fsum || !cnt) return fail(GH_ERR_INVALID_ARG, "fsum/cnt is NULL");
+  s = check_gspo_ws(num_segments, ws, ws_bytes);
+  if (s != GH_OK) return s;
   if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   GspoArgs g{static_cast<int>(N), logp, old_logp, ref_logp, mask, seg_id, num_segments, nullptr, 0.f, 0.f, 0.f,
-             1.0, 0, nullptr, nullptr, nullptr, nullptr, status};
-  cudaError_t e = run(K_GSPO_PARTIALS, st, [&] { return launch_gspo_partials(g, fsum, cnt, st); });
+             1.0, 0, nullptr, nullptr, nullptr, nullptr, nullptr, status};
+  cudaError_t e = run(K_GSPO_PARTIALS, st, [&] { return launch_gspo_partials(g, fsum, cnt, ws, st); });
   if (e != cudaSuccess) return cuda_fail(e, "GSPO partials launch");
   return GH_OK;
 }
@@ -504,7 +588,8 @@ gh_status gspo_segment_loss_from_partials(int64_t N, const float* logp, const fl
                                           const float* fsum_all, const int32_t* cnt_all, const float* seg_adv,
                                           float eps_low, float eps_high, float beta, double divisor,
                                           int32_t token_weighted, float* loss, float* seg_ratio, float* coef,
-                                          float* mean_logp, int32_t* status, void* stream) {
+                                          float* mean_logp, int32_t* num_clipped, int32_t* status, void* ws,
+                                          size_t ws_bytes, void* stream) {
   g_last_error.clear();
   gh_status s = check_gspo_common(N, logp, mask, seg_id, num_segments, status);
   if (s != GH_OK) return s;
@@ -512,25 +597,30 @@ gh_status gspo_segment_loss_from_partials(int64_t N, const float* logp, const fl
   if (s != GH_OK) return s;
   if (num_ranks < 1 || num_ranks > 4096) return fail(GH_ERR_INVALID_ARG, "num_ranks out of [1, 4096]");
   if (!fsum_all || !cnt_all) return fail(GH_ERR_INVALID_ARG, "fsum_all/cnt_all is NULL");
+  s = check_gspo_ws(num_segments, ws, ws_bytes);
+  if (s != GH_OK) return s;
   if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   GspoArgs g{static_cast<int>(N), logp, nullptr, beta != 0.f ? ref_logp : nullptr, mask, seg_id, num_segments,
-             seg_adv, eps_low, eps_high, beta, divisor, token_weighted, loss, seg_ratio, coef, mean_logp, status};
-  cudaError_t e = run(K_GSPO_FINISH, st, [&] { return launch_gspo_finish(g, num_ranks, fsum_all, cnt_all, st); });
+             seg_adv, eps_low, eps_high, beta, divisor, token_weighted, loss, seg_ratio, coef, mean_logp,
+             num_clipped, status};
+  cudaError_t e =
+      run(K_GSPO_FINISH, st, [&] { return launch_gspo_finish(g, num_ranks, fsum_all, cnt_all, ws, st); });
   if (e != cudaSuccess) return cuda_fail(e, "GSPO finish launch");
   return GH_OK;
 }
 
 // Backward body shared by the whole-vocabulary and the vocabulary-shard
 // entry points.  col_offset: global id of local column 0 (targets are global).
-// dh_partial: dH is an fp32 [N, D] partial over this vocabulary (no cast).
+// V_total: the whole vocabulary (it fixes the row chunks).  dh_partial: dH is
+// an fp32 [N, D] partial over this vocabulary (no cast).
 static gh_status backward_impl(const gh_head* head, const float* lse, const float* coef, const float* grad_out,
                                void* dH, float* dW, int32_t accumulate_dW, int32_t* status, void* ws,
-                               size_t ws_bytes, void* stream, int col_offset, bool dh_partial) {
+                               size_t ws_bytes, void* stream, int col_offset, int64_t V_total, bool dh_partial) {
   if (!status || !dW) return fail(GH_ERR_INVALID_ARG, "status/dW is NULL");
   if (head->N > 0 && (!lse || !coef || !dH)) return fail(GH_ERR_INVALID_ARG, "lse/coef/dH is NULL");
   if (!aligned16(dW) || (head->N > 0 && !aligned16(dH))) return fail(GH_ERR_INVALID_ARG, "dH/dW must be 16-byte aligned");
-  const size_t need = bwd_layout(head, nullptr).bytes;
+  const size_t need = bwd_layout(head, nullptr, V_total, dh_partial).bytes;
   if (need > 0 && (!ws || ws_bytes < need))
     return fail(GH_ERR_WORKSPACE, "backward workspace needs %zu bytes, got %zu", need, ws ? ws_bytes : size_t(0));
   if (!device_is_sm103()) return fail(GH_ERR_UNSUPPORTED, "current device is not an sm_103 (GB300) GPU");
@@ -543,64 +633,76 @@ static gh_status backward_impl(const gh_head* head, const float* lse, const floa
     }
     return GH_OK;
   }
-  BwdWs w = bwd_layout(head, ws);
+  BwdWs w = bwd_layout(head, ws, V_total, dh_partial);
   const int64_t Vp = ceil_div(V, VTILE) * VTILE;
-  for (int64_t b = 0; b < w.nblk; ++b) {
-    const int vb0 = static_cast<int>(b * w.vb);
-    const int width = static_cast<int>((Vp - vb0) < w.vb ? (Vp - vb0) : w.vb);
-    const int ldg = static_cast<int>(w.vb);
-    cudaError_t e;
-    if (head->dtype == GH_BF16) {
-      TcDlogitsArgs da{N, D, V, vb0, width, ldg, head->H, head->W, head->targets, lse, coef, grad_out, w.G, status,
-                       col_offset};
-      e = run(K_DLOGITS_TC, st, [&] { return launch_dlogits_tc(da, st); });
-      if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
-      int mode;
-      float* acc32 = w.acc32;
-      if (dh_partial) {
-        mode = b == 0 ? 0 : 1;  // fp32 partial accumulated in place
-        acc32 = static_cast<float*>(dH);
-      } else if (w.nblk == 1) {
-        mode = 3;
-      } else if (b == 0) {
-        mode = 0;
-      } else if (b == w.nblk - 1) {
-        mode = 2;
+  const bool bf16 = head->dtype == GH_BF16;
+  const size_t in_elt = bf16 ? 2 : 4;
+  const size_t dh_elt = (bf16 && !dh_partial) ? 2 : 4;
+  for (int64_t c = 0; c < w.nch; ++c) {
+    // rows [r0, r0 + n): this chunk's dH is finished over every block before
+    // the next chunk starts; its dW contribution is added to dW
+    const int64_t r0 = c * w.nc;
+    const int n = static_cast<int>((N - r0) < w.nc ? (N - r0) : w.nc);
+    const void* Hc = static_cast<const char*>(head->H) + static_cast<size_t>(r0) * D * in_elt;
+    const int32_t* yc = head->targets + r0;
+    const float* lse_c = lse + r0;
+    const float* coef_c = coef + r0;
+    void* dHc = static_cast<char*>(dH) + static_cast<size_t>(r0) * D * dh_elt;
+    const int acc_dW = (c > 0 || accumulate_dW) ? 1 : 0;
+    for (int64_t b = 0; b < w.nblk; ++b) {
+      const int vb0 = static_cast<int>(b * w.vb);
+      const int width = static_cast<int>((Vp - vb0) < w.vb ? (Vp - vb0) : w.vb);
+      const int ldg = static_cast<int>(w.vb);
+      cudaError_t e;
+      if (bf16) {
+        TcDlogitsArgs da{n, D, V, vb0, width, ldg, Hc, head->W, yc, lse_c, coef_c, grad_out, w.G, status,
+                         col_offset};
+        e = run(K_DLOGITS_TC, st, [&] { return launch_dlogits_tc(da, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
+        int mode;
+        float* acc32 = w.acc32;
+        if (dh_partial) {
+          mode = b == 0 ? 0 : 1;  // fp32 partial accumulated in place
+          acc32 = static_cast<float*>(dHc);
+        } else if (w.nblk == 1) {
+          mode = 3;
+        } else if (b == 0) {
+          mode = 0;
+        } else if (b == w.nblk - 1) {
+          mode = 2;
+        } else {
+          mode = 1;
+        }
+        TcDhArgs ha{n, D, V, vb0, width, ldg, w.G, head->W, mode, acc32, dHc, status};
+        TcDwArgs wa{n, D, V, vb0, width, ldg, w.G, Hc, acc_dW, dW, status};
+        if (dhdw_fused()) {
+          e = run(K_DHDW_TC, st, [&] { return launch_dhdw_tc(ha, wa, w.task_ctr, st); });
+          if (e != cudaSuccess) return cuda_fail(e, "dH/dW launch");
+        } else {
+          e = run(K_DH_TC, st, [&] { return launch_dh_tc(ha, st); });
+          if (e != cudaSuccess) return cuda_fail(e, "dH launch");
+          e = run(K_DW_TC, st, [&] { return launch_dw_tc(wa, st); });
+          if (e != cudaSuccess) return cuda_fail(e, "dW launch");
+        }
       } else {
-        mode = 1;
-      }
-      TcDhArgs ha{N, D, V, vb0, width, ldg, w.G, head->W, mode, acc32, dH, status};
-      TcDwArgs wa{N, D, V, vb0, width, ldg, w.G, head->H, accumulate_dW, dW, status};
-      if (dhdw_fused()) {
-        e = run(K_DHDW_TC, st, [&] { return launch_dhdw_tc(ha, wa, w.task_ctr, st); });
-        if (e != cudaSuccess) return cuda_fail(e, "dH/dW launch");
-      } else {
-        e = run(K_DH_TC, st, [&] { return launch_dh_tc(ha, st); });
+        const float* H = static_cast<const float*>(Hc);
+        const float* W = static_cast<const float*>(head->W);
+        float* G = static_cast<float*>(w.G);
+        F32DlogitsArgs da{n, D, V, vb0, width, ldg, H, W, yc, lse_c, coef_c, grad_out, G, col_offset};
+        e = run(K_DLOGITS_F32, st, [&] { return launch_dlogits_f32(da, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
+        const int real = static_cast<int>((V - vb0) < width ? (V - vb0) : width);
+        // dH[rows, D] (+)= G[:, :real] W[vb0:vb0+real, :]
+        F32GemmArgs ha{n, D, real, G, ldg, 1, W + static_cast<size_t>(vb0) * D, D, 1, static_cast<float*>(dHc), D,
+                       0, b > 0 ? 1 : 0, gemm_f32_par(n, D, real, w.slice_bytes), w.slices, 0};
+        e = run(K_GEMM_F32, st, [&] { return launch_gemm_f32(ha, st); });
         if (e != cudaSuccess) return cuda_fail(e, "dH launch");
-        e = run(K_DW_TC, st, [&] { return launch_dw_tc(wa, st); });
+        // dW[vb0 + v, :] (+)= sum over the chunk's rows i of G[i, v] H[i, :]
+        F32GemmArgs wa{real, D, n, G, 1, ldg, H, D, 1, dW, D, vb0, acc_dW, gemm_f32_par(real, D, n, w.slice_bytes),
+                       w.slices, 0};
+        e = run(K_GEMM_F32, st, [&] { return launch_gemm_f32(wa, st); });
         if (e != cudaSuccess) return cuda_fail(e, "dW launch");
       }
-    } else {
-      const float* H = static_cast<const float*>(head->H);
-      const float* W = static_cast<const float*>(head->W);
-      float* G = static_cast<float*>(w.G);
-      F32DlogitsArgs da{N, D, V, vb0, width, ldg, H, W, head->targets, lse, coef, grad_out, G, col_offset};
-      e = run(K_DLOGITS_F32, st, [&] { return launch_dlogits_f32(da, st); });
-      if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
-      const int real = static_cast<int>((V - vb0) < width ? (V - vb0) : width);
-      // dH[N, D] (+)= G[:, :real] W[vb0:vb0+real, :]
-      // the last block may be narrower than the widths the split was sized for: fewer slices then
-      const int ks_h = w.ks_dh > 1 ? gemm_f32_ksplit(N, D, real) : 1;
-      F32GemmArgs ha{N, D, real, G, ldg, 1, W + static_cast<size_t>(vb0) * D, D, 1, static_cast<float*>(dH), D, 0,
-                     b > 0 ? 1 : 0, ks_h < w.ks_dh ? ks_h : w.ks_dh, w.splitk};
-      e = run(K_GEMM_F32, st, [&] { return launch_gemm_f32(ha, st); });
-      if (e != cudaSuccess) return cuda_fail(e, "dH launch");
-      // dW[vb0 + v, :] (+)= sum_i G[i, v] H[i, :]
-      const int ks_w = w.ks_dw > 1 ? gemm_f32_ksplit(real, D, N) : 1;
-      F32GemmArgs wa{real, D, N, G, 1, ldg, H, D, 1, dW, D, vb0, accumulate_dW ? 1 : 0,
-                     ks_w < w.ks_dw ? ks_w : w.ks_dw, w.splitk};
-      e = run(K_GEMM_F32, st, [&] { return launch_gemm_f32(wa, st); });
-      if (e != cudaSuccess) return cuda_fail(e, "dW launch");
     }
   }
   return GH_OK;
@@ -612,7 +714,8 @@ gh_status grpo_head_backward(const gh_head* head, const float* lse, const float*
   g_last_error.clear();
   gh_status s = check_head(head);
   if (s != GH_OK) return s;
-  return backward_impl(head, lse, coef, grad_out, dH, dW, accumulate_dW, status, ws, ws_bytes, stream, 0, false);
+  return backward_impl(head, lse, coef, grad_out, dH, dW, accumulate_dW, status, ws, ws_bytes, stream, 0, head->V,
+                       false);
 }
 
 gh_status grpo_head_backward_shard(const gh_head* head, int64_t vocab_start, int64_t V_total, const float* lse,
@@ -626,7 +729,7 @@ gh_status grpo_head_backward_shard(const gh_head* head, int64_t vocab_start, int
   if (V_total > (int64_t(1) << 28) || vocab_start + head->V > V_total)
     return fail(GH_ERR_INVALID_ARG, "shard exceeds V_total");
   return backward_impl(head, lse, coef, grad_out, dH_partial, dW, accumulate_dW, status, ws, ws_bytes, stream,
-                       static_cast<int>(vocab_start), true);
+                       static_cast<int>(vocab_start), V_total, true);
 }
 
 gh_status grpo_dh_merge(int32_t num_shards, int64_t N, int64_t D, int32_t dtype, const float* dH_partials, void* dH,

@@ -141,6 +141,18 @@ struct F32DlogitsArgs {
 cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st);
 
 // C[row_off + m, n] (+)= sum_k A(m,k) B(k,n),  A(m,k) = A[m*sam + k*sak], B(k,n) = B[k*sbk + n*sbn]
+//
+// K is cut into slices of F32_SLICE (the last may be shorter).  Each output is
+// C0 + p_0 + p_1 + ... added left to right, where p_s is the fmaf chain of
+// slice s in increasing k and C0 is C (accumulate) or absent (C = p_0 + ...).
+// The slices run either one after the other inside each CTA (par <= 1, no
+// scratch) or `par` at a time in parallel CTAs that write their partials to
+// `scratch` [par, M, Nn], each wave then added to C in slice order by a
+// reduce kernel.  Both orders give the same bits, so `par` (chosen from the
+// output grid and the scratch available) never changes the result: it may
+// depend on M, and a data-parallel rank's dH rows or a vocabulary shard's dW
+// rows come out bitwise equal to the whole problem's.
+constexpr int F32_SLICE = 512;
 struct F32GemmArgs {
   int M, Nn, K;
   const float* A;
@@ -151,18 +163,16 @@ struct F32GemmArgs {
   long long ldc;
   int row_off;
   int accumulate;
-  // split K (small output grids): ksplit slices write partial [ksplit, M, Nn]
-  // products to `scratch`, then one kernel adds them to C in slice order
-  int ksplit;
-  float* scratch;
+  int par;         // slices run in parallel per wave (1 = all slices inside each CTA)
+  float* scratch;  // [par, M, Nn] partials when par > 1
+  int slice0;      // set by launch_gemm_f32: first slice of the current wave
 };
 cudaError_t launch_gemm_f32(const F32GemmArgs& a, cudaStream_t st);
-// K slices for an fp32 GEMM of this shape (a function of the shape only, so the
-// bits do not depend on the GPU) and the scratch they need
-int gemm_f32_ksplit(long long M, long long Nn, long long K);
+// slices to run in parallel for an M x Nn output with a K range, given
+// `scratch_bytes` of scratch (1 when the output grid alone fills the GPU)
+int gemm_f32_par(long long M, long long Nn, long long K, size_t scratch_bytes);
 // one more kernel launched inside a counted call (gh_launch_count)
 void count_extra_launch();
-constexpr size_t F32_SPLITK_SCRATCH_MAX = size_t(64) << 20;
 
 // --- loss kernels (loss_kernels.cu) -----------------------------------------
 cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const float* part_s, const float* zy,
@@ -178,8 +188,14 @@ struct ShardBounds {
 cudaError_t launch_merge_shards(int N, int V_total, int splits, const float* part_m, const float* part_s,
                                 const float* zy, const ShardBounds& sb, const int32_t* targets, const uint8_t* mask,
                                 float* logp, float* lse, int* status, cudaStream_t st);
+// GRPO loss.  `scratch` (nullable): grpo_loss_scratch_bytes(N) bytes from the
+// forward workspace; with it, and at most grpo_loss_scratch_seqs(N) sequences,
+// the loss runs one CTA per sequence, otherwise one CTA over all of them (the
+// same bits either way).
 cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_grpo* g, float* coef,
-                        float* loss3, int* status, cudaStream_t st);
+                        float* loss3, int* status, void* scratch, cudaStream_t st);
+size_t grpo_loss_scratch_bytes(int64_t N);
+int64_t grpo_loss_scratch_seqs(int64_t N);
 cudaError_t launch_grpo_totals(int num_seqs, const float* seq_policy, const float* seq_kl, const int32_t* seq_count,
                                int reduction, double norm, float beta, float* loss3, int* status, cudaStream_t st);
 struct GspoArgs {
@@ -198,11 +214,15 @@ struct GspoArgs {
   float* seg_ratio;
   float* coef;
   float* mean_logp;
+  int* num_clipped;
   int* status;
 };
-cudaError_t launch_gspo(const GspoArgs& g, cudaStream_t st);
-cudaError_t launch_gspo_partials(const GspoArgs& g, float* fsum, int32_t* cnt, cudaStream_t st);
-cudaError_t launch_gspo_finish(const GspoArgs& g, int R, const float* fsum_all, const int32_t* cnt_all,
+// GSPO seam steps.  `scratch` (nullable): gspo_scratch_bytes(num_segments)
+// bytes; with it one CTA per segment, otherwise one CTA (the same bits).
+size_t gspo_scratch_bytes(int num_segments);
+cudaError_t launch_gspo(const GspoArgs& g, void* scratch, cudaStream_t st);
+cudaError_t launch_gspo_partials(const GspoArgs& g, float* fsum, int32_t* cnt, void* scratch, cudaStream_t st);
+cudaError_t launch_gspo_finish(const GspoArgs& g, int R, const float* fsum_all, const int32_t* cnt_all, void* scratch,
                                cudaStream_t st);
 cudaError_t launch_advantage(const float* rewards, int num_seqs, int group_size, float eps, float* adv,
                              cudaStream_t st);

@@ -11,12 +11,16 @@
 //
 // The array is GH_NOALLOC_SCRATCH_BYTES (64 MiB); every GPU that loads this
 // library holds it until the process exits.  Its device address is looked up
-// once per device (with that device current) on the first call made there, so
-// that first call should come before any stream capture.  All calls share the
-// array: calls whose GPU work overlaps (different streams or threads) race on
-// it and must be serialised by the caller.  The array keeps the previous
-// call's contents; nothing in it has to start at zero, because the forward
-// writes every scratch slot it later reads within the same call.
+// on the first call made on each device (with that device current), so that
+// first call should come before any stream capture.  The address belongs to
+// the CUDA context it was looked up in: a later call from a different context
+// (after cudaDeviceReset, say) looks it up again.  All calls share the array:
+// calls whose GPU work overlaps (different streams or threads) race on it and
+// must be serialised by the caller.  The array keeps the previous call's
+// contents; nothing in it has to start at zero, because the forward writes
+// every scratch slot it later reads within the same call.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 #include <string>
@@ -31,9 +35,39 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[GH_NOALLOC_SCRA
 namespace {
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {nullptr};
+struct NoallocSlot {
+  void* ptr = nullptr;
+  unsigned long long ctx_id = 0;  // unique id of the context the address belongs to (0: unknown)
+};
+NoallocSlot g_noalloc_slot[64];
 
-// Device address of g_noalloc_scratch on the current device (looked up once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<F>(p);
+  return nullptr;
+}
+
+// Unique id (for the life of the process) of the calling thread's current
+// context, 0 when there is none or the driver cannot say.
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_cur || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call there and again when the current context has changed since.
 gh_status noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -46,16 +80,19 @@ gh_status noalloc_scratch(void** out) {
     return GH_ERR_UNSUPPORTED;
   }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoallocSlot& slot = g_noalloc_slot[dev];
+  const unsigned long long cur = current_context_id();
+  if (!slot.ptr || (cur != 0 && cur != slot.ctx_id)) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p) {
       set_error_message(std::string("cudaGetSymbolAddress(no-allocation scratch): ") + cudaGetErrorString(e));
       return GH_ERR_CUDA;
     }
-    g_noalloc_ptr[dev] = p;
+    slot.ptr = p;
+    slot.ctx_id = current_context_id();  // the lookup makes the device's primary context current
   }
-  *out = g_noalloc_ptr[dev];
+  *out = slot.ptr;
   return GH_OK;
 }
 

@@ -1,9 +1,10 @@
 // fp32 path (exact fp32 FMA on the CUDA cores, no TF32): logits + per-tile
 // (max, sum exp), dlogits recompute and the dH / dW GEMMs.
 //
-// Every logit z_ij and every GEMM output is one fmaf chain over k = 0, 1, ...
-// in increasing order, so its value does not depend on the tiling or on which
-// CTA computes it.  The kernels are register tiled: a thread keeps an 8 x 8
+// Every logit z_ij is one fmaf chain over k = 0, 1, ... in increasing order,
+// and every GEMM output is the left-to-right sum of such chains over fixed
+// 512-long K slices (F32_SLICE), so no value depends on the tiling, on which
+// CTA computes it or on how many slices run in parallel.  The kernels are register tiled: a thread keeps an 8 x 8
 // block of outputs, operands are staged in shared memory (double buffered,
 // the next K chunk is fetched into registers while the current one is used).
 //
@@ -216,44 +217,50 @@ __global__ void __launch_bounds__(L_THREADS, 2) f32_dlogits_kernel(
 // ---------------------------------------------------------------- GEMM
 // C[row_off + m, n] (+)= sum_k A(m, k) B(k, n) with B n-contiguous (B(k, n) =
 // B[k sbk + n]) and A either k-contiguous (A(m, k) = A[m sam + k]: dH = G W)
-// or m-contiguous (A(m, k) = A[m + k sak]: dW = G^T H).  128 x 128 tile per
-// 256-thread CTA; thread (tr, tc) = (t / 16, t % 16) owns rows 4tr.., 64+4tr..
-// and columns 4tc.., 64+4tc...
-constexpr int G_BM = 128, G_BN = 128, G_BK = 16;
-constexpr int G_PAD = G_BM + 4;
+// or m-contiguous (A(m, k) = A[m + k sak]: dW = G^T H).  A TILE x TILE output
+// tile per CTA of (TILE / 8)^2 threads (128: 256 threads for large grids, 64:
+// 64 threads for small ones); thread (tr, tc) owns rows 4tr.., TILE/2 + 4tr..
+// and columns 4tc.., TILE/2 + 4tc...  The tile size changes no output's
+// arithmetic.
+constexpr int G_BK = 16;
 
-template <bool A_KCONTIG, bool VEC>
-__global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
-  __shared__ __align__(16) float As[2][G_BK][G_PAD];
-  __shared__ __align__(16) float Bs[2][G_BK][G_PAD];
+template <int TILE, bool A_KCONTIG, bool VEC>
+__global__ void __launch_bounds__((TILE / 8) * (TILE / 8), TILE == 128 ? 2 : 4) f32_gemm_kernel(F32GemmArgs a) {
+  constexpr int THREADS = (TILE / 8) * (TILE / 8);
+  constexpr int TPR = TILE / 8;        // threads per row of the thread grid
+  constexpr int Q = TILE * 4 / THREADS;  // float4 of each operand chunk per thread
+  constexpr int F4R = TILE / 4;        // float4 per k-row of an MN-contiguous chunk
+  constexpr int PAD = TILE + 4;
+  __shared__ __align__(16) float As[2][G_BK][PAD];
+  __shared__ __align__(16) float Bs[2][G_BK][PAD];
   const int t = threadIdx.x;
-  const int tr = t >> 4, tc = t & 15;
-  const int m0 = blockIdx.y * G_BM, n0 = blockIdx.x * G_BN;
+  const int tr = t / TPR, tc = t % TPR;
+  const int m0 = blockIdx.y * TILE, n0 = blockIdx.x * TILE;
   float acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-  float4 pa[2], pb[2];
-  // A chunk: 128 x 16.  k-contiguous: element e = t + 256q -> row e/4, k 4(e%4).
-  // m-contiguous: e -> k e/32, rows 4(e%32)..
+  float4 pa[Q], pb[Q];
+  // A chunk: TILE x 16.  k-contiguous: element e = t + THREADS q -> row e/4,
+  // k 4(e%4).  m-contiguous: e -> k e/F4R, rows 4(e%F4R)..
   auto fetch = [&](int k0, int k_end) {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int e = t + 256 * q;
+    for (int q = 0; q < Q; ++q) {
+      const int e = t + THREADS * q;
       if (A_KCONTIG) {
         const int m = e >> 2, kq = (e & 3) * 4;
         const int gm = m0 + m;
         pa[q] = gm < a.M ? load4<VEC>(a.A + static_cast<long long>(gm) * a.sam, k0 + kq, k_end)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
       } else {
-        const int k = e >> 5, mq = (e & 31) * 4;
+        const int k = e / F4R, mq = (e % F4R) * 4;
         const int gk = k0 + k;
         pa[q] = gk < k_end ? load4<VEC>(a.A + static_cast<long long>(gk) * a.sak, m0 + mq, a.M)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      const int k = e >> 5, nq = (e & 31) * 4;
+      const int k = e / F4R, nq = (e % F4R) * 4;
       const int gk = k0 + k;
       pb[q] = gk < k_end ? load4<VEC>(a.B + static_cast<long long>(gk) * a.sbk, n0 + nq, a.Nn)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -261,8 +268,8 @@ __global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
   };
   auto stash = [&](int buf) {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int e = t + 256 * q;
+    for (int q = 0; q < Q; ++q) {
+      const int e = t + THREADS * q;
       if (A_KCONTIG) {
         const int m = e >> 2, kq = (e & 3) * 4;
         As[buf][kq + 0][m] = pa[q].x;
@@ -270,19 +277,45 @@ __global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
         As[buf][kq + 2][m] = pa[q].z;
         As[buf][kq + 3][m] = pa[q].w;
       } else {
-        const int k = e >> 5, mq = (e & 31) * 4;
+        const int k = e / F4R, mq = (e % F4R) * 4;
         *reinterpret_cast<float4*>(&As[buf][k][mq]) = pa[q];
       }
-      const int k = e >> 5, nq = (e & 31) * 4;
+      const int k = e / F4R, nq = (e % F4R) * 4;
       *reinterpret_cast<float4*>(&Bs[buf][k][nq]) = pb[q];
     }
   };
 
-  // K range of this slice (blockIdx.z) in G_BK steps; loads past k_end read 0
-  const int kslice = ((a.K + a.ksplit - 1) / a.ksplit + G_BK - 1) / G_BK * G_BK;
-  const int k_beg = blockIdx.z * kslice;
-  const int k_end = min(a.K, k_beg + kslice);
-  const int nk = k_end > k_beg ? (k_end - k_beg + G_BK - 1) / G_BK : 0;
+  // Slices [s_beg, s_end): all of them inside this CTA, or slice slice0 +
+  // blockIdx.z of a parallel wave.  Loads past k_end read 0.
+  const bool wave = a.scratch != nullptr;
+  const int nslices = a.K > 0 ? (a.K + F32_SLICE - 1) / F32_SLICE : 1;
+  const int s_beg = wave ? a.slice0 + static_cast<int>(blockIdx.z) : 0;
+  const int s_end = wave ? s_beg + 1 : nslices;
+  const int k_beg = s_beg * F32_SLICE;
+  const int k_end = min(a.K, s_end * F32_SLICE);
+  constexpr int CPS = F32_SLICE / G_BK;  // K chunks per slice
+  static_assert(F32_SLICE % G_BK == 0, "slices are whole K chunks");
+  const int nk = k_end > k_beg ? (k_end - k_beg + G_BK - 1) / G_BK : 1;
+
+  // slice s finished: C = p_0 (first slice, no accumulate) or C + p_s; in a
+  // parallel wave the partial goes to this slice's scratch slab instead
+  auto flush = [&](int s) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int gm = m0 + (i < 4 ? 4 * tr : TILE / 2 + 4 * tr) + (i & 3);
+      if (gm >= a.M) continue;
+      float* crow = wave ? a.scratch + (static_cast<long long>(blockIdx.z) * a.M + gm) * a.Nn
+                         : a.C + (static_cast<long long>(a.row_off) + gm) * a.ldc;
+      const bool add = !wave && (s > 0 || a.accumulate);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int gn = n0 + (j < 4 ? 4 * tc : TILE / 2 + 4 * tc) + (j & 3);
+        if (gn >= a.Nn) continue;
+        crow[gn] = add ? crow[gn] + acc[i][j] : acc[i][j];
+      }
+    }
+  };
+
   fetch(k_beg, k_end);
   stash(0);
   __syncthreads();
@@ -292,9 +325,9 @@ __global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
 #pragma unroll
     for (int k = 0; k < G_BK; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * tr]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][64 + 4 * tr]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][TILE / 2 + 4 * tr]);
       const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][4 * tc]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][64 + 4 * tc]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][TILE / 2 + 4 * tc]);
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -302,36 +335,31 @@ __global__ void __launch_bounds__(256, 2) f32_gemm_kernel(F32GemmArgs a) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
+    if ((kc + 1) % CPS == 0 || kc + 1 == nk) {
+      flush(s_beg + kc / CPS);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    }
     if (kc + 1 < nk) {
       stash(buf ^ 1);
       __syncthreads();
     }
   }
-  const bool partial = a.ksplit > 1;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int gm = m0 + (i < 4 ? 4 * tr : 64 + 4 * tr) + (i & 3);
-    if (gm >= a.M) continue;
-    float* crow = partial ? a.scratch + (static_cast<long long>(blockIdx.z) * a.M + gm) * a.Nn
-                          : a.C + (static_cast<long long>(a.row_off) + gm) * a.ldc;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int gn = n0 + (j < 4 ? 4 * tc : 64 + 4 * tc) + (j & 3);
-      if (gn >= a.Nn) continue;
-      crow[gn] = (!partial && a.accumulate) ? (crow[gn] + acc[i][j]) : acc[i][j];
-    }
-  }
 }
 
-// C[row_off + m, n] = (accumulate ? C : 0) + sum over slices z = 0, 1, ... of scratch[z, m, n]
-__global__ void __launch_bounds__(256) f32_splitk_reduce_kernel(F32GemmArgs a) {
+// One parallel wave of `count` slices starting at slice0, added to C in slice
+// order: C = (first slice and no accumulate ? p_0 : C + p_0) + p_1 + ...
+__global__ void __launch_bounds__(256) f32_slice_reduce_kernel(F32GemmArgs a, int count) {
   const long long total = static_cast<long long>(a.M) * a.Nn;
+  const bool start = a.slice0 == 0 && !a.accumulate;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long m = i / a.Nn, n = i % a.Nn;
     float* c = a.C + (a.row_off + m) * a.ldc + n;
-    float v = a.accumulate ? *c : 0.f;
-    for (int z = 0; z < a.ksplit; ++z) v += a.scratch[z * total + i];
+    float v = start ? a.scratch[i] : *c + a.scratch[i];
+    for (int z = 1; z < count; ++z) v += a.scratch[z * total + i];
     *c = v;
   }
 }
@@ -368,45 +396,79 @@ cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-int gemm_f32_ksplit(long long M, long long Nn, long long K) {
-  // aim for at least 256 CTAs of 128 x 128 outputs, slices of at least 512 in K,
-  // at most 8 slices, scratch within F32_SPLITK_SCRATCH_MAX
-  const long long tiles = ceil_div(M, G_BM) * ceil_div(Nn, G_BN);
-  if (tiles <= 0 || tiles >= 256 || K < 1024) return 1;
-  long long s = ceil_div(256, tiles);
-  s = s < 8 ? s : 8;
-  s = s < K / 512 ? s : K / 512;
-  while (s > 1 && static_cast<size_t>(s * M * Nn) * 4 > F32_SPLITK_SCRATCH_MAX) --s;
-  return s < 1 ? 1 : static_cast<int>(s);
+// Output tile of an M x Nn fp32 GEMM: 128 x 128 unless that leaves fewer
+// CTAs than a GB300 has SMs (152; a constant, so nothing here depends on the
+// machine), then 64 x 64.
+static int gemm_f32_tile(long long M, long long Nn) {
+  return ceil_div(M, 128) * ceil_div(Nn, 128) < 152 ? 64 : 128;
 }
 
-cudaError_t launch_gemm_f32(const F32GemmArgs& a, cudaStream_t st) {
-  if (a.M <= 0 || a.Nn <= 0) return cudaSuccess;
-  if (a.sbn != 1 || (a.sak != 1 && a.sam != 1)) return cudaErrorInvalidValue;
-  if (a.ksplit < 1 || (a.ksplit > 1 && !a.scratch)) return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>(ceil_div(a.Nn, G_BN)), static_cast<unsigned>(ceil_div(a.M, G_BM)),
-            static_cast<unsigned>(a.ksplit));
+int gemm_f32_par(long long M, long long Nn, long long K, size_t scratch_bytes) {
+  // about 304 CTAs (two on each of a GB300's 152 SMs), at most one per slice,
+  // within the scratch; constants, so workspace sizes do not depend on the
+  // machine that asks
+  const long long slices = K > 0 ? ceil_div(K, F32_SLICE) : 1;
+  const int tile = gemm_f32_tile(M, Nn);
+  const long long tiles = ceil_div(M, tile) * ceil_div(Nn, tile);
+  const long long want = 304;
+  if (slices <= 1 || tiles <= 0 || tiles >= want || M <= 0 || Nn <= 0) return 1;
+  long long p = ceil_div(want, tiles);
+  p = p < slices ? p : slices;
+  const long long fit = static_cast<long long>(scratch_bytes / (static_cast<size_t>(M) * Nn * 4));
+  p = p < fit ? p : fit;
+  return p > 1 ? static_cast<int>(p) : 1;
+}
+
+template <int TILE>
+static void gemm_f32_launch(const F32GemmArgs& a, unsigned count, bool kc, bool vec, cudaStream_t st) {
+  constexpr int THREADS = (TILE / 8) * (TILE / 8);
+  dim3 grid(static_cast<unsigned>(ceil_div(a.Nn, TILE)), static_cast<unsigned>(ceil_div(a.M, TILE)), count);
+  if (kc) {
+    if (vec)
+      f32_gemm_kernel<TILE, true, true><<<grid, THREADS, 0, st>>>(a);
+    else
+      f32_gemm_kernel<TILE, true, false><<<grid, THREADS, 0, st>>>(a);
+  } else {
+    if (vec)
+      f32_gemm_kernel<TILE, false, true><<<grid, THREADS, 0, st>>>(a);
+    else
+      f32_gemm_kernel<TILE, false, false><<<grid, THREADS, 0, st>>>(a);
+  }
+}
+
+cudaError_t launch_gemm_f32(const F32GemmArgs& a0, cudaStream_t st) {
+  if (a0.M <= 0 || a0.Nn <= 0) return cudaSuccess;
+  if (a0.sbn != 1 || (a0.sak != 1 && a0.sam != 1)) return cudaErrorInvalidValue;
+  const int slices = a0.K > 0 ? static_cast<int>(ceil_div(a0.K, F32_SLICE)) : 1;
+  F32GemmArgs a = a0;
+  a.slice0 = 0;
+  int par = a.par < slices ? a.par : slices;
+  if (par <= 1 || !a.scratch) {
+    par = 1;
+    a.scratch = nullptr;
+  }
   const bool kc = a.sak == 1;
   const long long lda = kc ? a.sam : a.sak;
   const bool vec = aligned16(a.A) && aligned16(a.B) && lda % 4 == 0 && a.sbk % 4 == 0;
-  if (kc) {
-    if (vec)
-      f32_gemm_kernel<true, true><<<grid, 256, 0, st>>>(a);
+  const int tile = gemm_f32_tile(a.M, a.Nn);
+  const long long total = static_cast<long long>(a.M) * a.Nn;
+  const unsigned rblocks = static_cast<unsigned>(ceil_div(total, 256) < 4096 ? ceil_div(total, 256) : 4096);
+  bool first = true;
+  for (int s0 = 0; s0 < (par > 1 ? slices : 1); s0 += par) {
+    const int count = par > 1 ? (slices - s0 < par ? slices - s0 : par) : 1;
+    a.slice0 = s0;
+    if (tile == 64)
+      gemm_f32_launch<64>(a, static_cast<unsigned>(count), kc, vec, st);
     else
-      f32_gemm_kernel<true, false><<<grid, 256, 0, st>>>(a);
-  } else {
-    if (vec)
-      f32_gemm_kernel<false, true><<<grid, 256, 0, st>>>(a);
-    else
-      f32_gemm_kernel<false, false><<<grid, 256, 0, st>>>(a);
-  }
-  if (a.ksplit > 1) {
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const long long total = static_cast<long long>(a.M) * a.Nn;
-    const unsigned blocks = static_cast<unsigned>(ceil_div(total, 256) < 4096 ? ceil_div(total, 256) : 4096);
-    f32_splitk_reduce_kernel<<<blocks, 256, 0, st>>>(a);
-    count_extra_launch();
+      gemm_f32_launch<128>(a, static_cast<unsigned>(count), kc, vec, st);
+    if (!first) count_extra_launch();
+    first = false;
+    if (par > 1) {
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      f32_slice_reduce_kernel<<<rblocks, 256, 0, st>>>(a, count);
+      count_extra_launch();
+    }
   }
   return cudaGetLastError();
 }

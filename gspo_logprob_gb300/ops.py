@@ -50,18 +50,29 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
 
 
 class _Workspace:
-    """Grow-only scratch buffer per device, reused by consecutive calls (not
-    safe for calls that overlap on different streams)."""
+    """Grow-only scratch buffer per device, reused by consecutive calls.
+
+    Calls whose GPU work overlaps on different streams must not share it (pass
+    ``workspace=``).  Used from several streams one after the other, the buffer
+    is marked as in use on each of them (``record_stream``), so that when it is
+    replaced by a larger one torch's caching allocator does not hand its memory
+    to other work before the kernels queued on those streams have finished."""
 
     def __init__(self):
         self._buf = {}
 
     def get(self, dev: torch.device, nbytes: int) -> torch.Tensor:
         key = (dev.type, dev.index)
-        b = self._buf.get(key)
-        if b is None or b.numel() < nbytes:
+        cur = torch.cuda.current_stream(dev)
+        entry = self._buf.get(key)
+        if entry is None or entry[0].numel() < nbytes:
             b = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
-            self._buf[key] = b
+            entry = (b, {cur.cuda_stream})
+            self._buf[key] = entry
+        b, seen = entry
+        if cur.cuda_stream not in seen:
+            b.record_stream(cur)
+            seen.add(cur.cuda_stream)
         return b
 
     def clear(self):
@@ -69,6 +80,28 @@ class _Workspace:
 
 
 WORKSPACE = _Workspace()
+
+_MAX_SEGMENTS = 16384
+_SEAM_WS = {}
+
+
+def _seam_workspace(dev: torch.device) -> torch.Tensor:
+    """Scratch of the GSPO seam calls: one buffer per device, sized for the
+    most segments a call takes, allocated once (its address never changes, so
+    CUDA-graph captures of these calls stay valid).  Calls that overlap on
+    different streams must pass their own ``workspace=``."""
+    key = (dev.type, dev.index)
+    b = _SEAM_WS.get(key)
+    if b is None:
+        b = torch.empty(int(_lib().gspo_segment_workspace_size(_MAX_SEGMENTS)), dtype=torch.uint8, device=dev)
+        _SEAM_WS[key] = b
+    return b
+
+
+def _seam_ws(dev, num_segments: int, workspace: Optional[torch.Tensor]):
+    nbytes = int(_lib().gspo_segment_workspace_size(int(num_segments)))
+    ws = _caller_workspace(workspace, nbytes) if workspace is not None else _seam_workspace(dev)
+    return ws, nbytes
 
 
 def _caller_workspace(ws: torch.Tensor, nbytes: int) -> torch.Tensor:
@@ -103,6 +136,10 @@ def backward_workspace_bytes(head: GhHead) -> int:
     return int(_lib().grpo_head_backward_workspace_size(ctypes.byref(head)))
 
 
+def backward_shard_workspace_bytes(head: GhHead, V_total: int) -> int:
+    return int(_lib().grpo_head_backward_shard_workspace_size(ctypes.byref(head), int(V_total)))
+
+
 def new_status(dev) -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -118,20 +155,22 @@ def raise_on_status(status: torch.Tensor, allow: int = 0) -> int:
 def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=None, seq_id=None,
                       num_seqs: int = 0, eps_low: float = 0.2, eps_high: float = 0.2, beta: float = 0.0,
                       reduction: str = "token_mean", norm: float = 0.0, delta: float = 0.0,
-                      ratio_level: str = "token", seq_totals: bool = False, row_tile: int = 0,
-                      want_coef: bool = True, status: Optional[torch.Tensor] = None, out: Optional[dict] = None,
-                      workspace: Optional[torch.Tensor] = None):
+                      ratio_level: str = "token", seq_totals: bool = False, clip_count: bool = False,
+                      row_tile: int = 0, want_coef: bool = True, status: Optional[torch.Tensor] = None,
+                      out: Optional[dict] = None, workspace: Optional[torch.Tensor] = None):
     """Selected-token log-probs and LSE; with ``old_logp`` given, also the GRPO
     loss (loss, policy_loss, kl) and coef = d loss / d logp.  ``delta`` > 0
     caps the unclipped ratio (two-sided clip); ``ratio_level="sequence"`` uses
     one ratio per sequence; ``seq_totals`` also returns the per-sequence totals
-    (seq_policy, seq_kl, seq_count) for a data-parallel reduction.
+    (seq_policy, seq_kl, seq_count) for a data-parallel reduction;
+    ``clip_count`` returns ``num_clipped`` (int32 [1]), the active tokens whose
+    policy gradient the clip cuts off.
 
     ``workspace``: a caller-owned CUDA byte buffer of at least
     forward_workspace_bytes(head) bytes; by default the binding's shared,
     grow-only buffer is used.  The shared buffer serves one stream at a time:
-    calls whose GPU work overlaps on different streams must each pass their
-    own.  A call captured into a CUDA graph keeps the workspace address it was
+    calls whose GPU work overlaps, e.g. on different streams, must each pass
+    their own.  A call captured into a CUDA graph keeps the workspace address it was
     given, so pass your own buffer when capturing (the shared one may be
     replaced by a larger one later).
 
@@ -157,13 +196,19 @@ def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=
             totals = (torch.empty(num_seqs, dtype=_F32, device=dev), torch.empty(num_seqs, dtype=_F32, device=dev),
                       torch.empty(num_seqs, dtype=torch.int32, device=dev))
             out.update(seq_policy=totals[0], seq_kl=totals[1], seq_count=totals[2])
+        clipped = None
+        if clip_count:
+            clipped = out.get("num_clipped") if out.get("num_clipped") is not None else \
+                torch.empty(1, dtype=torch.int32, device=dev)
+            out.update(num_clipped=clipped)
         g = GhGrpo(old_logp=old_logp.data_ptr(), ref_logp=ref_logp.data_ptr() if ref_logp is not None else None,
                    adv=adv.data_ptr(), seq_id=seq_id.data_ptr(), num_seqs=num_seqs,
                    reduction=_abi.REDUCTIONS[reduction], eps_low=eps_low, eps_high=eps_high, beta=beta,
                    delta=float(delta), norm=float(norm), ratio_level=_abi.RATIO_LEVELS[ratio_level], reserved=0,
                    seq_policy=totals[0].data_ptr() if totals else None,
                    seq_kl=totals[1].data_ptr() if totals else None,
-                   seq_count=totals[2].data_ptr() if totals else None)
+                   seq_count=totals[2].data_ptr() if totals else None,
+                   num_clipped=clipped.data_ptr() if clipped is not None else None)
         if want_coef:
             coef = out.get("coef") if out.get("coef") is not None else torch.empty(N, dtype=_F32, device=dev)
         loss3 = out.get("loss3") if out.get("loss3") is not None else torch.empty(3, dtype=_F32, device=dev)
@@ -251,7 +296,7 @@ def grpo_head_backward_shard(H, W_shard, targets, mask, lse, coef, *, vocab_star
     else:
         _need(dW, "dW", _F32, (V, D))
     st = new_status(dev) if status is None else status
-    nbytes = backward_workspace_bytes(head)
+    nbytes = backward_shard_workspace_bytes(head, V_total)
     ws = WORKSPACE.get(dev, nbytes)
     code = _lib().grpo_head_backward_shard(ctypes.byref(head), int(vocab_start), int(V_total), _ptr(lse), _ptr(coef),
                                            _ptr(grad_out), _ptr(dHp), _ptr(dW), 1 if accumulate_dW else 0, _ptr(st),
@@ -293,10 +338,14 @@ def grpo_loss_from_sequence_totals(seq_policy, seq_kl, seq_count, *, reduction: 
 
 def gspo_segment_loss(logp, old_logp, mask, seg_id, num_segments: int, seg_adv, *, eps_low: float,
                       eps_high: float, divisor: float, token_weighted: bool = False, ref_logp=None,
-                      beta: float = 0.0, status: Optional[torch.Tensor] = None):
+                      beta: float = 0.0, status: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None):
     """GSPO sequence-level loss over packed documents (optionally with a
     per-segment mean k3 KL weighted by beta); returns loss [1], seg_ratio [S],
-    coef [N], mean_logp [1] and status."""
+    coef [N], mean_logp [1], num_clipped [1] (live segments whose policy
+    gradient the clip cuts off) and status.  ``workspace``: a caller-owned
+    CUDA byte buffer of gspo_segment_workspace_size(num_segments) bytes; by
+    default a fixed per-device buffer."""
     N = logp.numel()
     _need(logp, "logp", _F32, (N,))
     _need(old_logp, "old_logp", _F32, (N,))
@@ -310,17 +359,19 @@ def gspo_segment_loss(logp, old_logp, mask, seg_id, num_segments: int, seg_adv, 
     ratio = torch.empty(num_segments, dtype=_F32, device=dev)
     coef = torch.empty(N, dtype=_F32, device=dev)
     mean_logp = torch.empty(1, dtype=_F32, device=dev)
+    clipped = torch.empty(1, dtype=torch.int32, device=dev)
     st = new_status(dev) if status is None else status
+    ws, nbytes = _seam_ws(dev, num_segments, workspace)
     code = _lib().gspo_segment_loss(N, _ptr(logp), _ptr(old_logp), _ptr(ref_logp), _ptr(mask), _ptr(seg_id),
                                     num_segments, _ptr(seg_adv), eps_low, eps_high, float(beta), float(divisor),
                                     1 if token_weighted else 0, _ptr(loss), _ptr(ratio), _ptr(coef), _ptr(mean_logp),
-                                    _ptr(st), _stream(dev))
+                                    _ptr(clipped), _ptr(st), _ptr(ws), nbytes, _stream(dev))
     _abi.check(code, "gspo_segment_loss")
-    return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, status=st)
+    return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, num_clipped=clipped, status=st)
 
 
 def gspo_segment_partials(logp, old_logp, mask, seg_id, num_segments: int, *, ref_logp=None,
-                          status: Optional[torch.Tensor] = None):
+                          status: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
     """One sequence-parallel rank's GSPO partials: fsum [2S + 1], cnt [S + 1]."""
     N = logp.numel()
     _need(logp, "logp", _F32, (N,))
@@ -331,15 +382,18 @@ def gspo_segment_partials(logp, old_logp, mask, seg_id, num_segments: int, *, re
     fsum = torch.empty(2 * num_segments + 1, dtype=_F32, device=dev)
     cnt = torch.empty(num_segments + 1, dtype=torch.int32, device=dev)
     st = new_status(dev) if status is None else status
+    ws, nbytes = _seam_ws(dev, num_segments, workspace)
     code = _lib().gspo_segment_partials(N, _ptr(logp), _ptr(old_logp), _ptr(ref_logp), _ptr(mask), _ptr(seg_id),
-                                        num_segments, _ptr(fsum), _ptr(cnt), _ptr(st), _stream(dev))
+                                        num_segments, _ptr(fsum), _ptr(cnt), _ptr(st), _ptr(ws), nbytes,
+                                        _stream(dev))
     _abi.check(code, "gspo_segment_partials")
     return dict(fsum=fsum, cnt=cnt, status=st)
 
 
 def gspo_segment_loss_from_partials(logp, mask, seg_id, num_segments: int, fsum_all, cnt_all, seg_adv, *,
                                     eps_low: float, eps_high: float, divisor: float, token_weighted: bool = False,
-                                    ref_logp=None, beta: float = 0.0, status: Optional[torch.Tensor] = None):
+                                    ref_logp=None, beta: float = 0.0, status: Optional[torch.Tensor] = None,
+                                    workspace: Optional[torch.Tensor] = None):
     """GSPO loss from the ranks' gathered partials ([R, 2S + 1], [R, S + 1]);
     coef for this rank's tokens."""
     N = logp.numel()
@@ -357,22 +411,28 @@ def gspo_segment_loss_from_partials(logp, mask, seg_id, num_segments: int, fsum_
     ratio = torch.empty(num_segments, dtype=_F32, device=dev)
     coef = torch.empty(N, dtype=_F32, device=dev)
     mean_logp = torch.empty(1, dtype=_F32, device=dev)
+    clipped = torch.empty(1, dtype=torch.int32, device=dev)
     st = new_status(dev) if status is None else status
+    ws, nbytes = _seam_ws(dev, num_segments, workspace)
     code = _lib().gspo_segment_loss_from_partials(N, _ptr(logp), _ptr(ref_logp), _ptr(mask), _ptr(seg_id),
                                                   num_segments, R, _ptr(fsum_all), _ptr(cnt_all), _ptr(seg_adv),
                                                   eps_low, eps_high, float(beta), float(divisor),
                                                   1 if token_weighted else 0, _ptr(loss), _ptr(ratio), _ptr(coef),
-                                                  _ptr(mean_logp), _ptr(st), _stream(dev))
+                                                  _ptr(mean_logp), _ptr(clipped), _ptr(st), _ptr(ws), nbytes,
+                                                  _stream(dev))
     _abi.check(code, "gspo_segment_loss_from_partials")
-    return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, status=st)
+    return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, num_clipped=clipped, status=st)
 
 
 def grpo_head_backward(H, W, targets, mask, lse, coef, *, grad_out=None, dH=None, dW=None,
                        accumulate_dW: bool = False, row_tile: int = 0, status: Optional[torch.Tensor] = None,
                        workspace: Optional[torch.Tensor] = None):
     """dH [N, D] (dtype of H) and dW [V, D] fp32 from each row's LSE and coef.
-    ``workspace`` as in grpo_head_forward, at least backward_workspace_bytes(head)
-    bytes."""
+
+    ``workspace``: a caller-owned CUDA byte buffer of at least
+    backward_workspace_bytes(head) bytes; by default the binding's shared,
+    grow-only buffer is used, which serves one stream at a time: calls whose
+    GPU work overlaps, e.g. on different streams, must each pass their own."""
     head = make_head(H, W, targets, mask, row_tile)
     dev = H.device
     N, D, V = head.N, head.D, head.V

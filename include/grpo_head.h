@@ -23,9 +23,14 @@
  *
  * Conventions shared by every entry point:
  *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
- *    never allocates or frees device memory, and keeps none between calls apart
- *    from the fixed scratch array of grpo_head_forward_noalloc (scratch space is
- *    otherwise the caller's `ws` buffer, sized by the *_workspace_size calls).
+ *    never allocates or frees device memory and keeps no device data between
+ *    calls, apart from the fixed scratch array of grpo_head_forward_noalloc
+ *    (scratch space is otherwise the caller's `ws` buffer, sized by the
+ *    *_workspace_size calls).  Host state it does keep for the life of the
+ *    process: per-device launch set-up (kernel attributes, the number of CTA
+ *    pairs that fit, device properties, the no-allocation array's address),
+ *    tuning knobs read once from the environment, the calling thread's last
+ *    error message, and the process-wide instrumentation counters below.
  *  - All work is enqueued asynchronously on `stream` (a cudaStream_t passed as
  *    void*; NULL = the legacy default stream).  Nothing synchronises.  The work
  *    is kernels and asynchronous memsets only, so these calls can be captured
@@ -122,12 +127,35 @@ typedef struct {
                              tokens of the policy term (before the normaliser)           */
   float* seq_kl;          /* optional out [num_seqs]: same for the KL term               */
   int32_t* seq_count;     /* optional out [num_seqs]: active tokens of each sequence     */
+  int32_t* num_clipped;   /* optional out [1]: active tokens whose policy gradient the
+                             clip (or the delta cap) cuts off, act = 0 below: the
+                             clipped-token count behind the usual clip fraction       */
 } gh_grpo;
 
-/* Bytes of scratch `ws` grpo_head_forward needs for this problem. */
+/*
+ * Bytes of scratch `ws` grpo_head_forward needs for this problem: the split
+ * partials and target logits of the log-prob, and per-sequence slots of the
+ * GRPO loss for up to max(64, N / 8) sequences (capped at 16384).  With more
+ * sequences than slots the loss runs on one CTA instead of one CTA per
+ * sequence, with the same results, bit for bit.
+ */
 size_t grpo_head_forward_workspace_size(const gh_head* head);
-/* Bytes of scratch `ws` grpo_head_backward needs for this problem. */
+/*
+ * Bytes of scratch `ws` grpo_head_backward needs for this problem: one
+ * dlogits block (bf16: at most 16384 vocabulary columns, plus an fp32 dH
+ * accumulator when the vocabulary spans several blocks; fp32: at most 1024
+ * columns, plus partials of the GEMMs' K slices that run in parallel) for a
+ * chunk of rows.  The rows per chunk keep this at most three quarters of
+ * N * V * 2 bytes (the size of the bf16 [N, V] logits), except on problems too
+ * small for it: a chunk holds at least min(N, 128) rows (bf16; 64 for fp32) of
+ * at least one 256-column tile.
+ */
 size_t grpo_head_backward_workspace_size(const gh_head* head);
+/*
+ * Bytes of scratch grpo_head_backward_shard needs for the vocabulary shard
+ * `head` of a V_total-column vocabulary (0 for invalid arguments).
+ */
+size_t grpo_head_backward_shard_workspace_size(const gh_head* head, int64_t V_total);
 
 /*
  * Forward: selected-token log-prob and LSE for every row, and, when `grpo` is
@@ -203,8 +231,11 @@ gh_status grpo_logprob_merge(int64_t N, int64_t V_total, int32_t num_shards, con
  * per-row values (from grpo_logprob_merge and the loss), identical on every
  * rank.  Writes dW [head->V, D] fp32 for the shard's rows (added to dW when
  * accumulate_dW) and dH_partial [N, D] fp32 = G_shard W_shard; the shards'
- * partials summed in shard order (grpo_dh_merge) give dH.  Workspace: at least
- * grpo_head_backward_workspace_size(head) bytes.
+ * partials summed in shard order (grpo_dh_merge) give dH.  The shard's dW rows
+ * are bitwise the rows grpo_head_backward gives on the whole vocabulary (both
+ * add dW over the same row chunks, which depend on V_total, not on the
+ * shard).  Workspace: at least grpo_head_backward_shard_workspace_size(head,
+ * V_total) bytes.
  */
 gh_status grpo_head_backward_shard(const gh_head* head, int64_t vocab_start, int64_t V_total, const float* lse,
                                    const float* coef, const float* grad_out, float* dH_partial, float* dW,
@@ -245,14 +276,19 @@ gh_status grpo_loss_from_sequence_totals(int32_t num_seqs, const float* seq_poli
  * an unused tail (whose mask must be 0).  Segments with n_s = 0 contribute 0
  * and report seg_ratio 1.  ref_logp may be NULL when beta == 0.  Outputs:
  * loss [1], seg_ratio [num_segments], coef [N], mean_logp [1] (the
- * new_logprobs metric: mean active logp); seg_ratio / mean_logp may be NULL.
- * No scratch memory is needed.
+ * new_logprobs metric: mean active logp), num_clipped [1] (live segments
+ * whose policy gradient the clip cuts off, act_s = 0); seg_ratio, mean_logp
+ * and num_clipped may be NULL.
+ * ws: gspo_segment_workspace_size(num_segments) bytes of scratch, or NULL.
+ * With it each segment gets its own CTA; without it one CTA does every
+ * segment.  Both give the same results, bit for bit.
  */
+size_t gspo_segment_workspace_size(int32_t num_segments);
 gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp, const float* ref_logp,
                             const uint8_t* mask, const int32_t* seg_id, int32_t num_segments, const float* seg_adv,
                             float eps_low, float eps_high, float beta, double divisor, int32_t token_weighted,
-                            float* loss, float* seg_ratio, float* coef, float* mean_logp, int32_t* status,
-                            void* stream);
+                            float* loss, float* seg_ratio, float* coef, float* mean_logp, int32_t* num_clipped,
+                            int32_t* status, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * GSPO under sequence parallelism (Fast-LLM PR #554, What / Correctness: the
@@ -266,19 +302,20 @@ gh_status gspo_segment_loss(int64_t N, const float* logp, const float* old_logp,
  * order ([num_ranks, 2S + 1] and [num_ranks, S + 1]) and each calls
  * gspo_segment_loss_from_partials for its own tokens: the partials are summed
  * over ranks in rank order (no float all-reduce, so the result does not depend
- * on the collective's topology), then loss, seg_ratio, mean_logp and this
- * rank's coef follow as in gspo_segment_loss.  With one rank the result is
- * bitwise gspo_segment_loss's.
+ * on the collective's topology), then loss, seg_ratio, mean_logp, num_clipped
+ * and this rank's coef follow as in gspo_segment_loss.  With one rank the
+ * result is bitwise gspo_segment_loss's.  ws as in gspo_segment_loss.
  */
 gh_status gspo_segment_partials(int64_t N, const float* logp, const float* old_logp, const float* ref_logp,
                                 const uint8_t* mask, const int32_t* seg_id, int32_t num_segments, float* fsum,
-                                int32_t* cnt, int32_t* status, void* stream);
+                                int32_t* cnt, int32_t* status, void* ws, size_t ws_bytes, void* stream);
 gh_status gspo_segment_loss_from_partials(int64_t N, const float* logp, const float* ref_logp, const uint8_t* mask,
                                           const int32_t* seg_id, int32_t num_segments, int32_t num_ranks,
                                           const float* fsum_all, const int32_t* cnt_all, const float* seg_adv,
                                           float eps_low, float eps_high, float beta, double divisor,
                                           int32_t token_weighted, float* loss, float* seg_ratio, float* coef,
-                                          float* mean_logp, int32_t* status, void* stream);
+                                          float* mean_logp, int32_t* num_clipped, int32_t* status, void* ws,
+                                          size_t ws_bytes, void* stream);
 
 /*
  * Backward of the head given each row's LSE and coef (from grpo_head_forward
@@ -286,7 +323,11 @@ gh_status gspo_segment_loss_from_partials(int64_t N, const float* logp, const fl
  *   G_ij = g coef_i (1[j = y_i] - exp(z_ij - LSE_i))   (g = *grad_out, or 1 if NULL)
  * and dH = G W (fp32 accumulation over blocks in increasing vocabulary order,
  * written in `dtype`), dW = G^T H (fp32; added to dW when accumulate_dW != 0,
- * e.g. across micro-batches).  dH [N, D] in dtype; dW [V, D] fp32.
+ * e.g. across micro-batches).  dH [N, D] in dtype; dW [V, D] fp32.  When the
+ * vocabulary is narrow next to the block and accumulator rows, the rows are
+ * processed in chunks (see grpo_head_backward_workspace_size), each adding its
+ * dW contribution in chunk order; the chunks depend on N, D, dtype and V only.
+ * A row's dH does not depend on the chunks or on the other rows of the batch.
  */
 gh_status grpo_head_backward(const gh_head* head, const float* lse, const float* coef,
                              const float* grad_out, void* dH, float* dW, int32_t accumulate_dW,
@@ -318,7 +359,9 @@ gh_status grpo_group_advantage(const float* rewards, int32_t num_seqs, int32_t g
  * rejected with GH_ERR_INVALID_ARG and a message in gh_last_error() before
  * any GPU work.  The array's device address is looked up on the first call
  * made on each device (with that device current), so make that first call
- * before any stream capture.  All calls share the one array and it keeps the
+ * before any stream capture; it is looked up again when a call comes from a
+ * different CUDA context than the one it was found in (after
+ * cudaDeviceReset, for example).  All calls share the one array and it keeps the
  * last call's contents (nothing in it needs to start at zero): calls whose GPU
  * work overlaps in time, e.g. on two streams, race on it and must be
  * serialised by the caller.

@@ -353,6 +353,7 @@ def gspo_loss(logp, old, mask, seg_id, num_segments: int, seg_adv, eps_low: floa
     rho = np.ones(num_segments)
     ell = np.zeros(num_segments)
     g = np.zeros(num_segments)                           # policy part of d loss / d logp, per active token
+    seg_act = np.zeros(num_segments, dtype=bool)         # the policy term moves with rho (not cut by the clip)
     kb = np.zeros(num_segments)                          # KL part scale, per active token
     loss = 0.0
     abs_terms = 0.0
@@ -364,6 +365,7 @@ def gspo_loss(logp, old, mask, seg_id, num_segments: int, seg_adv, eps_low: floa
         u, v = rho[s] * A[s], c * A[s]
         ell[s] = -min(u, v)
         act = True if u <= v else (1.0 - eps_low <= rho[s] <= 1.0 + eps_high)
+        seg_act[s] = act
         omega = float(n[s]) if token_weighted else 1.0
         term = ell[s] + (beta * K[s] / n[s] if use_kl else 0.0)
         loss += omega * term / divisor
@@ -378,7 +380,7 @@ def gspo_loss(logp, old, mask, seg_id, num_segments: int, seg_adv, eps_low: floa
             if use_kl:
                 coef[i] += kb[s] * (1.0 - math.exp(rf[i] - logp[i]))
     mean_logp = lp_sum / act_tokens if act_tokens > 0 else 0.0
-    return dict(loss=loss, seg_ratio=rho, seg_loss=ell, coef=coef, counts=n,
+    return dict(loss=loss, seg_ratio=rho, seg_loss=ell, coef=coef, counts=n, seg_act=seg_act,
                 seg_sum=S, seg_kl=K, mean_logp=mean_logp, abs_terms=abs_terms)
 
 

@@ -60,7 +60,7 @@ def test_struct_layout_matches_c(lib, tmp_path):
 
 
 def test_host_only_calls(lib):
-    assert lib.gh_abi_version() == 104
+    assert lib.gh_abi_version() == 106
     assert lib.gh_status_string(0) == b"GH_OK"
     assert lib.gh_status_string(3) == b"GH_ERR_WORKSPACE"
     assert lib.gh_kernel_kind_name(0) == b"fwd_logits_lse_tc"
@@ -75,27 +75,43 @@ def _head(N=1000, D=256, V=5000, dtype=0, row_tile=0, aligned=True):
 
 def test_workspace_sizes(lib):
     h = _head(N=1000, D=256, V=5000)
-    # forward: two [splits, N] fp32 partial arrays + zy [N]; splits = ceil(5000/256) = 20
+    # forward: two [splits, N] fp32 partial arrays + zy [N]; splits = ceil(5000/256) = 20;
+    # then the GRPO loss's four per-sequence arrays for max(64, N/8) = 125 sequences
+    # and 256 bytes of counters
     fw = lib.grpo_head_forward_workspace_size(ctypes.byref(h))
     al = lambda x: (x + 255) // 256 * 256
-    assert fw == 2 * al(20 * 1000 * 4) + al(1000 * 4)
-    # backward (bf16): one block of all 5120 padded columns, no dH accumulator
+    assert fw == 2 * al(20 * 1000 * 4) + al(1000 * 4) + 4 * al(125 * 4) + 256
+    # backward (bf16): one block of all 5120 padded columns, no dH accumulator;
+    # all 1000 rows would take 10.24 MB against 3/4 of N*V*2 = 7.5 MB, so the rows
+    # go in two chunks of 512 (whole 256-row tiles)
     bw = lib.grpo_head_backward_workspace_size(ctypes.byref(h))
-    assert bw == al(1000 * 5120 * 2) + 256          # + the tile counter of the fused dH/dW launch
-    # a vocabulary of two 16384-column blocks adds the fp32 dH accumulator
+    assert bw == al(512 * 5120 * 2) + 256          # + the tile counter of the fused dH/dW launch
+    assert bw <= 0.75 * 1000 * 5000 * 2
+    # a vocabulary of two 16384-column blocks adds the fp32 dH accumulator of a chunk
     h3 = _head(N=1000, D=256, V=20000)
-    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h3)) == al(1000 * 16384 * 2) + al(1000 * 256 * 4) + 256
-    # a single-block vocabulary needs no accumulator
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h3)) == al(512 * 16384 * 2) + al(512 * 256 * 4) + 256
+    # a wide vocabulary keeps all rows in one chunk
+    h6 = _head(N=8192, D=4096, V=151936)
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h6)) == \
+        al(8192 * 16384 * 2) + al(8192 * 4096 * 4) + 256
+    # fewer rows than one tile: a single chunk whatever the ratio
     h2 = _head(N=64, D=64, V=500)
     assert lib.grpo_head_backward_workspace_size(ctypes.byref(h2)) == al(64 * 512 * 2) + 256
-    # fp32, N = D = 1024, V = 4096: the G block [1024, 4096] fp32, the counter, and the
-    # split-K scratch of dH (8 x 8 output tiles < 256 -> 4 slices of K = 4096: 4 x 1024 x 1024
-    # fp32); dW ([4096, 1024] = 256 tiles) is not split
+    # fp32, N = D = 1024, V = 4096: 1024-column blocks, all rows (4 MB of the 6.3 MB
+    # budget); the 64 output tiles of each GEMM would run two K slices in parallel,
+    # but two [1024, 1024] fp32 partials do not fit what is left, so none is allocated
     h4 = _head(N=1024, D=1024, V=4096, dtype=1)
-    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h4)) == al(1024 * 4096 * 4) + 256 + al(4 * 1024 * 1024 * 4)
-    # a large fp32 problem needs no split
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h4)) == al(1024 * 1024 * 4) + 256
+    # tiny fp32 problem (N=256, V=500): 64-row chunks keep the block at half of N*V*2
+    h7 = _head(N=256, D=64, V=500, dtype=1)
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h7)) == al(64 * 512 * 4) + 256
+    # a large fp32 problem needs no parallel slices
     h5 = _head(N=8192, D=4096, V=4096, dtype=1)
-    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h5)) == al(8192 * 4096 * 4) + 256
+    assert lib.grpo_head_backward_workspace_size(ctypes.byref(h5)) == al(8192 * 1024 * 4) + 256
+    # a vocabulary shard sizes its chunks by the whole vocabulary and needs no dH accumulator
+    hs = _head(N=1000, D=256, V=2560)
+    assert lib.grpo_head_backward_shard_workspace_size(ctypes.byref(hs), 5000) == al(512 * 2560 * 2) + 256
+    assert lib.grpo_head_backward_shard_workspace_size(ctypes.byref(hs), 2000) == 0      # V_total < V
     # invalid problem -> 0
     assert lib.grpo_head_forward_workspace_size(ctypes.byref(_head(D=12))) == 0
 
@@ -136,14 +152,20 @@ def test_no_gpu_fails_loudly(lib):
 
 def test_gspo_and_advantage_validation(lib):
     st = lib.gspo_segment_loss(10, 0x100, 0x100, None, 0x100, 0x100, 0, 0x100, 0.2, 0.2, 0.0, 1.0, 0, 0x100, None,
-                               0x100, None, 0x100, None)
+                               0x100, None, None, 0x100, None, 0, None)
     assert st == 1 and b"num_segments" in lib.gh_last_error()
     st = lib.gspo_segment_loss(10, 0x100, 0x100, None, 0x100, 0x100, 4, 0x100, 0.2, 0.2, 0.0, 0.0, 0, 0x100, None,
-                               0x100, None, 0x100, None)
+                               0x100, None, None, 0x100, None, 0, None)
     assert st == 1 and b"divisor" in lib.gh_last_error()
     st = lib.gspo_segment_loss(10, 0x100, 0x100, None, 0x100, 0x100, 4, 0x100, 0.2, 0.2, 0.1, 1.0, 0, 0x100, None,
-                               0x100, None, 0x100, None)
+                               0x100, None, None, 0x100, None, 0, None)
     assert st == 1 and b"ref_logp" in lib.gh_last_error()
+    # a workspace smaller than gspo_segment_workspace_size is refused
+    need = lib.gspo_segment_workspace_size(4)
+    assert need > 0 and lib.gspo_segment_workspace_size(0) == 0
+    st = lib.gspo_segment_loss(10, 0x100, 0x100, None, 0x100, 0x100, 4, 0x100, 0.2, 0.2, 0.0, 1.0, 0, 0x100, None,
+                               0x100, None, None, 0x100, 0x10000, need - 1, None)
+    assert st == 3 and b"GSPO workspace" in lib.gh_last_error()
     st = lib.grpo_group_advantage(0x100, 10, 4, 1e-4, 0x100, 0x100, None)
     assert st == 1 and b"multiple" in lib.gh_last_error()
 
@@ -179,3 +201,31 @@ def test_shard_argument_validation(lib):
     starts = (ctypes.c_int64 * 3)(0, 3000, 5000)
     assert lib.grpo_logprob_merge(100, 5000, 2, starts, 0x100, 0x100, 0x100, 0x100, 0x100, 0x100, 0x100, 0x100,
                                   None) == 1
+
+
+# workloads (N, D, V, dtype) whose workspaces must stay below the bf16 [N, V]
+# logits they never form: the five configurations, in both dtypes where the
+# path exists, and the packed-GSPO shapes
+_MEMORY_CASES = [
+    ("tiny fp32 GRPO", 256, 64, 500, 1),
+    ("tiny GRPO in bf16", 256, 64, 500, 0),
+    ("selective logp bf16", 4096, 256, 5000, 0),
+    ("selective logp fp32", 4096, 256, 5000, 1),
+    ("bf16 GRPO small", 1024, 1024, 4096, 0),
+    ("fp32 GRPO small", 1024, 1024, 4096, 1),
+    ("bf16 GSPO packed", 16384, 2048, 32000, 0),
+    ("bf16 8B-vocab micro-batch", 8192, 4096, 151936, 0),
+]
+
+
+@pytest.mark.parametrize("name,N,D,V,dtype", _MEMORY_CASES)
+def test_extra_memory_below_logits(lib, name, N, D, V, dtype):
+    # peak extra device memory of a forward + backward is the larger of the two
+    # workspaces (the library allocates nothing else): at most 3/4 of N*V*2
+    # (the method's memory claim is that [N, V] is never materialised)
+    h = _head(N=N, D=D, V=V, dtype=dtype)
+    fw = lib.grpo_head_forward_workspace_size(ctypes.byref(h))
+    bw = lib.grpo_head_backward_workspace_size(ctypes.byref(h))
+    ratio = max(fw, bw) / (N * V * 2)
+    print(f"{name}: forward {fw} B, backward {bw} B, {ratio:.3f} of N*V*2")
+    assert ratio <= 0.75 + 256 / (N * V * 2) + 1e-9

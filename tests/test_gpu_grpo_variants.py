@@ -15,9 +15,9 @@ from gpu_helpers import BF16_LOSS_REL, assert_grad_bf16, bf16_np, dev_head, dev_
 pytestmark = pytest.mark.gpu
 
 
-def _prepare(old_noise):
+def _prepare(old_noise, dtype=None):
     cfg = CONFIGS[2]
-    w = make_workload(cfg, old_noise=old_noise)
+    w = make_workload(cfg, old_noise=old_noise, dtype=dtype)
     H, W = host_head(w)
     lp, _, _ = oracle.selected_logprob(H, W, w["targets"], w["mask"])
     w["old"] = (lp + w["u_old"]).astype(np.float32)
@@ -122,17 +122,20 @@ def test_data_parallel_split_is_bitwise_identical(gpu_lib, reduction, ratio_leve
         assert torch.equal(r["logp"].view(torch.int32), whole["logp"][sl].view(torch.int32))
 
 
-def test_data_parallel_straddling_group_and_rank_ordered_dW(gpu_lib):
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_data_parallel_straddling_group_and_rank_ordered_dW(gpu_lib, dtype):
     # two "ranks" own whole sequences of one batch, cut inside an advantage
     # group (8 sequences, G = 8, cut after 3).  Each rank normalises advantages
     # from the gathered rewards of all sequences, runs forward + backward on its
     # tokens with the global normaliser and a fresh dW, and the dW partials are
-    # summed in rank order.  That sum is bitwise the single-process accumulation
-    # over the same two pieces (dW of piece 0 stored, piece 1 added), each
-    # rank's dH rows are bitwise the whole-batch dH rows, and dW matches the
-    # oracle over the whole batch.
+    # summed in rank order.  Each rank's dH rows are bitwise the whole-batch dH
+    # rows (a row's dH depends on neither the batch nor the row chunks, and the
+    # fp32 GEMMs' K slices do not depend on the rows either); the rank-ordered
+    # sum is the plain fp32 sum of the partials, the same bits on a repeat; and
+    # dW matches the oracle over the whole batch.
     import gspo_logprob_gb300 as g
-    cfg, w, H, W = _prepare(0.05)    # ratios inside the clip band: no gradient switches at its edges
+    from gpu_helpers import FP32_GRAD_ABS
+    cfg, w, H, W = _prepare(0.05, dtype)    # ratios inside the clip band: no gradient switches at its edges
     Hd, Wd, y, m = dev_head(w)
     S, G = w["num_seqs"], w["group_size"]
     seq = w["seq_id"]
@@ -156,15 +159,19 @@ def test_data_parallel_straddling_group_and_rank_ordered_dW(gpu_lib):
         bw = g.grpo_head_backward(*args, fw["lse"], fw["coef"])
         pieces.append((sl, args, fw, bw))
     reduced = g.grpo_dh_merge(torch.stack([p[3]["dW"] for p in pieces]), dtype=torch.float32)
-    # the same pieces accumulated in one process
-    acc = None
-    for k, (sl, args, fw, _) in enumerate(pieces):
-        acc = g.grpo_head_backward(*args, fw["lse"], fw["coef"], dW=acc, accumulate_dW=k > 0)["dW"]
+    again = g.grpo_dh_merge(torch.stack([p[3]["dW"] for p in pieces]), dtype=torch.float32)
     torch.cuda.synchronize()
-    assert torch.equal(reduced.view(torch.int32), acc.view(torch.int32))
-    for sl, _, _, bw in pieces:
-        assert torch.equal(bw["dH"].view(torch.int16), whole_bw["dH"][sl].view(torch.int16))
+    assert torch.equal(reduced, pieces[0][3]["dW"] + pieces[1][3]["dW"])
+    assert torch.equal(reduced.view(torch.int32), again.view(torch.int32))
+    iv = torch.int16 if dtype == "bf16" else torch.int32
+    for sl, _, fw, bw in pieces:
+        assert torch.equal(fw["lse"].view(torch.int32), whole_fw["lse"][sl].view(torch.int32))
+        assert torch.equal(bw["dH"].view(iv), whole_bw["dH"][sl].view(iv))
     o = oracle.forward_backward(H, W, w["targets"], w["mask"], seq, w["adv"].astype(np.float64), S,
                                 w["old"].astype(np.float64), w["ref"].astype(np.float64), cfg.eps_low, cfg.eps_high,
                                 cfg.beta, norm=norm)
-    assert_grad_bf16(reduced.cpu().numpy(), o["dW"], "dW reduced over ranks")
+    if dtype == "bf16":
+        assert_grad_bf16(reduced.cpu().numpy(), o["dW"], "dW reduced over ranks")
+    else:
+        assert np.max(np.abs(reduced.cpu().numpy() - o["dW"])) <= FP32_GRAD_ABS
+        assert np.max(np.abs(whole_bw["dH"].cpu().numpy() - o["dH"])) <= FP32_GRAD_ABS

@@ -183,3 +183,33 @@ def test_kl_term_coef_is_derivative():
             lp[i] -= 2 * h
             dn = oracle.gspo_loss(lp, *args)["loss"]
             assert abs((up - dn) / (2 * h) - res["coef"][i]) < 1e-7
+
+
+def test_segment_act_by_clip_region():
+    # act_s (the segment's policy term moves with rho) in each region of the
+    # clip, for one-token segments with log-ratio log(rho): inside the band
+    # always; above 1 + eps_high only for A < 0; below 1 - eps_low only for A > 0
+    rho = np.array([1.0, 1.5, 1.5, 0.5, 0.5, 1.1])
+    adv = np.array([0.7, 0.7, -0.7, 0.7, -0.7, -0.3])
+    want = np.array([True, False, True, True, False, True])
+    logp = np.full(6, -1.0)
+    old = logp - np.log(rho)
+    res = oracle.gspo_loss(logp, old, np.ones(6, np.uint8), np.arange(6), 6, adv, 0.2, 0.28, 6.0)
+    assert np.array_equal(res["seg_act"], want)
+    assert np.array_equal(res["coef"] != 0, want)            # the cut-off segments carry no gradient
+
+
+def test_segment_act_matches_token_act_for_one_token_segments():
+    # one-token segments: the segment's act is the token-level GRPO act,
+    # computed by the oracle's separate token code
+    rng = np.random.default_rng(9)
+    N = 200
+    logp = -rng.uniform(0.1, 4, N)
+    old = logp + rng.uniform(-0.6, 0.6, N)
+    adv = rng.standard_normal(N)
+    mask = np.ones(N, dtype=np.uint8)
+    seg = np.arange(N)
+    g = oracle.gspo_loss(logp, old, mask, seg, N, adv, 0.2, 0.28, 5.0)
+    t = oracle.grpo_loss(logp, old, None, mask, seg, adv, N, 0.2, 0.28, 0.0, "fixed", 5.0)
+    assert 0 < int((~g["seg_act"]).sum()) < N
+    assert np.array_equal(g["seg_act"], t["act"] > 0)
