@@ -34,12 +34,25 @@ __device__ __forceinline__ float wsum(float v) {
 // Returns the LSE in warp 0's lanes (meaningless in the others).
 __device__ __forceinline__ float fold_splits(int N, int splits, const float* __restrict__ part_m,
                                              const float* __restrict__ part_s, float (*red)[33]) {
+  // Loads are issued FOLD_BATCH splits at a time (all in flight together) and
+  // then used in increasing split order, so the sums keep the order above.
+  constexpr int FOLD_BATCH = 16;
   const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x * 32 + lane;
   const bool ok = i < N;
   float mx = -INFINITY;
-  if (ok)
-    for (int k = g; k < splits; k += 8) mx = fmaxf(mx, part_m[static_cast<size_t>(k) * N + i]);
+  if (ok) {
+    for (int k0 = g; k0 < splits; k0 += 8 * FOLD_BATCH) {
+      float v[FOLD_BATCH];
+#pragma unroll
+      for (int b = 0; b < FOLD_BATCH; ++b) {
+        const int k = k0 + 8 * b;
+        v[b] = k < splits ? __ldg(part_m + static_cast<size_t>(k) * N + i) : -INFINITY;
+      }
+#pragma unroll
+      for (int b = 0; b < FOLD_BATCH; ++b) mx = fmaxf(mx, v[b]);
+    }
+  }
   red[g][lane] = mx;
   __syncthreads();
   float M = red[0][lane];
@@ -48,9 +61,17 @@ __device__ __forceinline__ float fold_splits(int N, int splits, const float* __r
   __syncthreads();
   float s = 0.f;
   if (ok && M != -INFINITY) {
-    for (int k = g; k < splits; k += 8) {
-      const float mk = part_m[static_cast<size_t>(k) * N + i];
-      if (mk != -INFINITY) s += part_s[static_cast<size_t>(k) * N + i] * expf(mk - M);
+    for (int k0 = g; k0 < splits; k0 += 8 * FOLD_BATCH) {
+      float vm[FOLD_BATCH], vs[FOLD_BATCH];
+#pragma unroll
+      for (int b = 0; b < FOLD_BATCH; ++b) {
+        const int k = k0 + 8 * b;
+        vm[b] = k < splits ? __ldg(part_m + static_cast<size_t>(k) * N + i) : -INFINITY;
+        vs[b] = k < splits ? __ldg(part_s + static_cast<size_t>(k) * N + i) : 0.f;
+      }
+#pragma unroll
+      for (int b = 0; b < FOLD_BATCH; ++b)
+        if (vm[b] != -INFINITY) s += vs[b] * expf(vm[b] - M);
     }
   }
   red[g][lane] = s;
