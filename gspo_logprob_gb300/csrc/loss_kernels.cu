@@ -153,6 +153,9 @@ __global__ void __launch_bounds__(256) merge_shards_kernel(int N, int V_total, i
 // memory, and gives the same bits.
 constexpr int LB = 512;
 constexpr int LW = LB / 32;
+// calls of at most this many tokens get coef from the folding CTA rather than
+// from a separate token-parallel kernel
+constexpr int LAST_CTA_COEF_MAX = 4096;
 
 struct Red {
   float f0, f1, f2;
@@ -487,6 +490,20 @@ __global__ void __launch_bounds__(LB) grpo_loss_kernel(GrpoP p, GrpoScr g) {
     }
   }
   __syncthreads();
+  if (!SINGLE && p.coef && !p.direct && p.N <= LAST_CTA_COEF_MAX) {
+    // a small call: the folding CTA writes coef itself (one launch fewer)
+    const int flag = s_flag;
+    for (int i = t; i < p.N; i += LB) {
+      float c = 0.f;
+      if (p.mask[i] && !flag) {
+        const int s = p.seq_id[i];
+        c = grpo_coef_of(p, i, p.adv[s], ld_other<true>(g.R + s), grpo_weight(p, s_scale, ld_other<true>(g.n + s)),
+                         lo, hi);
+      }
+      p.coef[i] = c;
+    }
+    return;
+  }
   if (SINGLE && p.coef && !p.direct) {
     // coef_i = w_i (-A r act + beta (1 - exp(d))); at the sequence level r and
     // act are the sequence's (every token of a sequence has the same weight,
@@ -919,7 +936,7 @@ cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_
     if (e != cudaSuccess) return e;
     grpo_loss_kernel<false><<<loss_grid(S), LB, 0, st>>>(p, gs);
     e = cudaGetLastError();
-    if (e != cudaSuccess || !coef || p.direct || N <= 0) return e;
+    if (e != cudaSuccess || !coef || p.direct || N <= LAST_CTA_COEF_MAX) return e;
     const unsigned blocks = static_cast<unsigned>(std::min<int64_t>(ceil_div(N, 256), 4 * num_sms()));
     grpo_coef_kernel<<<blocks, 256, 0, st>>>(p, gs);
     count_extra_launch();

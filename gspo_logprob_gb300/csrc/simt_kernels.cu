@@ -49,9 +49,12 @@ __device__ __forceinline__ float4 load4(const float* __restrict__ row, int c, in
   return v;
 }
 
+// ROWS x 256 logits tile of a CTA of ROWS * 4 threads (64: 256 threads, the
+// default; 32: 128 threads, for small dlogits grids)
+template <int ROWS>
 struct LogitsSmem {
-  float A[2][L_BK][L_APAD];  // H chunk, k-major: A[k][row]
-  float B[2][L_BK][L_BPAD];  // W chunk, k-major: B[k][col]
+  float A[2][L_BK][ROWS + 4];  // H chunk, k-major: A[k][row]
+  float B[2][L_BK][L_BPAD];    // W chunk, k-major: B[k][col]
 };
 
 // Column of output j (0..7) of lane l within the 256-wide tile.
@@ -59,10 +62,12 @@ __device__ __forceinline__ int lcol(int lane, int j) { return (j < 4 ? 4 * lane 
 
 // z[r][j] = sum_k H[r0 + 8w + r, k] W[c0 + lcol(lane, j), k] (zero for rows >= N
 // or columns >= V).  Thread t fetches one float4 of H (row t/4, k 4(t%4)) and
-// four of W (column (t + 256q)/4) per K chunk.
-template <bool VEC>
+// QB of W (column (t + THREADS q)/4) per K chunk.
+template <bool VEC, int ROWS = L_BM>
 __device__ __forceinline__ void logits_tile(const float* __restrict__ H, const float* __restrict__ W, int N, int D,
-                                            int V, int r0, int c0, LogitsSmem& sm, float z[8][8]) {
+                                            int V, int r0, int c0, LogitsSmem<ROWS>& sm, float z[8][8]) {
+  constexpr int THREADS = ROWS * 4;
+  constexpr int QB = L_BN * 4 / THREADS;  // float4 of the W chunk per thread
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
 #pragma unroll
   for (int r = 0; r < 8; ++r)
@@ -71,24 +76,24 @@ __device__ __forceinline__ void logits_tile(const float* __restrict__ H, const f
   const int ar = t >> 2, akq = (t & 3) * 4;
   const int agr = r0 + ar;
   const float* hrow = H + static_cast<size_t>(agr < N ? agr : 0) * D;
-  const float* wrow[4];
-  int bc[4];
+  const float* wrow[QB];
+  int bc[QB];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    bc[q] = (t + 256 * q) >> 2;
+  for (int q = 0; q < QB; ++q) {
+    bc[q] = (t + THREADS * q) >> 2;
     const int gc = c0 + bc[q];
     wrow[q] = W + static_cast<size_t>(gc < V ? gc : 0) * D;
   }
   const bool arow_ok = agr < N;
-  bool bcol_ok[4];
+  bool bcol_ok[QB];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) bcol_ok[q] = c0 + bc[q] < V;
+  for (int q = 0; q < QB; ++q) bcol_ok[q] = c0 + bc[q] < V;
 
-  float4 pa, pb[4];
+  float4 pa, pb[QB];
   auto fetch = [&](int k0) {
     pa = arow_ok ? load4<VEC>(hrow, k0 + akq, D) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < QB; ++q)
       pb[q] = bcol_ok[q] ? load4<VEC>(wrow[q], k0 + akq, D) : make_float4(0.f, 0.f, 0.f, 0.f);
   };
   auto stash = [&](int buf) {
@@ -97,7 +102,7 @@ __device__ __forceinline__ void logits_tile(const float* __restrict__ H, const f
     sm.A[buf][akq + 2][ar] = pa.z;
     sm.A[buf][akq + 3][ar] = pa.w;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < QB; ++q) {
       sm.B[buf][akq + 0][bc[q]] = pb[q].x;
       sm.B[buf][akq + 1][bc[q]] = pb[q].y;
       sm.B[buf][akq + 2][bc[q]] = pb[q].z;
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(L_THREADS, 2) f32_fwd_kernel(const float* __re
                                                               const int* __restrict__ targets, int N, int D, int V,
                                                               int row_tile, int col_offset, float* part_m,
                                                               float* part_s, float* zy) {
-  __shared__ __align__(16) LogitsSmem sm;
+  __shared__ __align__(16) LogitsSmem<L_BM> sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.y;
   const int c0 = split * L_BN;
@@ -179,20 +184,20 @@ __global__ void __launch_bounds__(L_THREADS, 2) f32_fwd_kernel(const float* __re
   }
 }
 
-// grid: (ceil(N / 64), width / 256).  G[i, lc] = g coef_i (1[col = y_i] - exp(z - LSE_i))
+// grid: (ceil(N / ROWS), width / 256).  G[i, lc] = g coef_i (1[col = y_i] - exp(z - LSE_i))
 // for the block's local column lc (0 at padded columns).
-template <bool VEC>
-__global__ void __launch_bounds__(L_THREADS, 2) f32_dlogits_kernel(
+template <bool VEC, int ROWS>
+__global__ void __launch_bounds__(ROWS * 4, 2) f32_dlogits_kernel(
     const float* __restrict__ H, const float* __restrict__ W, const int* __restrict__ targets,
     const float* __restrict__ lse, const float* __restrict__ coef, const float* __restrict__ grad_out, int N, int D,
     int V, int vb0, int ldg, int col_offset, float* G) {
-  __shared__ __align__(16) LogitsSmem sm;
+  __shared__ __align__(16) LogitsSmem<ROWS> sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blockIdx.x * L_BM;
+  const int r0 = blockIdx.x * ROWS;
   const int lc0 = blockIdx.y * L_BN;
   const int c0 = vb0 + lc0;
   float z[8][8];
-  logits_tile<VEC>(H, W, N, D, V, r0, c0, sm, z);
+  logits_tile<VEC, ROWS>(H, W, N, D, V, r0, c0, sm, z);
   const float g = grad_out ? *grad_out : 1.f;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
@@ -382,17 +387,27 @@ cudaError_t launch_fwd_f32(const F32FwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int ROWS>
+static void dlogits_f32_launch(const F32DlogitsArgs& a, bool vec, cudaStream_t st) {
+  dim3 grid(static_cast<unsigned>(ceil_div(a.N, ROWS)), static_cast<unsigned>(a.width / L_BN));
+  if (vec)
+    f32_dlogits_kernel<true, ROWS><<<grid, ROWS * 4, 0, st>>>(a.H, a.W, a.targets, a.lse, a.coef, a.grad_out, a.N,
+                                                               a.D, a.V, a.vb0, a.ldg, a.col_offset, a.G);
+  else
+    f32_dlogits_kernel<false, ROWS><<<grid, ROWS * 4, 0, st>>>(a.H, a.W, a.targets, a.lse, a.coef, a.grad_out, a.N,
+                                                                a.D, a.V, a.vb0, a.ldg, a.col_offset, a.G);
+}
+
 cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st) {
   if (a.N <= 0) return cudaSuccess;
   if (a.width % L_BN != 0 || a.ldg % 4 != 0 || !aligned16(a.G)) return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>(ceil_div(a.N, L_BM)), static_cast<unsigned>(a.width / L_BN));
   const bool vec = a.D % 4 == 0 && aligned16(a.H) && aligned16(a.W);
-  if (vec)
-    f32_dlogits_kernel<true><<<grid, L_THREADS, 0, st>>>(a.H, a.W, a.targets, a.lse, a.coef, a.grad_out, a.N, a.D,
-                                                          a.V, a.vb0, a.ldg, a.col_offset, a.G);
+  // 32-row tiles (twice the CTAs) when 64-row tiles would leave SMs idle; the
+  // tile changes no value
+  if (ceil_div(a.N, L_BM) * (a.width / L_BN) < 152)
+    dlogits_f32_launch<32>(a, vec, st);
   else
-    f32_dlogits_kernel<false><<<grid, L_THREADS, 0, st>>>(a.H, a.W, a.targets, a.lse, a.coef, a.grad_out, a.N, a.D,
-                                                           a.V, a.vb0, a.ldg, a.col_offset, a.G);
+    dlogits_f32_launch<L_BM>(a, vec, st);
   return cudaGetLastError();
 }
 

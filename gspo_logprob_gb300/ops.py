@@ -12,6 +12,7 @@ Device-side status: each call returns (or fills) an int32 status tensor; use
 from __future__ import annotations
 
 import ctypes
+import functools
 from typing import Optional
 
 import torch
@@ -25,6 +26,37 @@ _F32 = torch.float32
 
 def _lib():
     return _abi.load()
+
+
+_NVTX_OK = [None]  # None: not tried yet
+
+
+def _nvtx_usable() -> bool:
+    if _NVTX_OK[0] is None:
+        try:
+            torch.cuda.nvtx.range_push("gh.probe")
+            torch.cuda.nvtx.range_pop()
+            _NVTX_OK[0] = torch.cuda.is_available()
+        except Exception:  # a torch build without NVTX: no ranges
+            _NVTX_OK[0] = False
+    return _NVTX_OK[0]
+
+
+def _nvtx(fn):
+    """Bracket a binding entry point with an NVTX range of its name, so a
+    profiler timeline groups each call's kernels (no cost without a profiler)."""
+    name = "gh." + fn.__name__
+
+    @functools.wraps(fn)
+    def wrapped(*args, **kwargs):
+        if not _nvtx_usable():
+            return fn(*args, **kwargs)
+        torch.cuda.nvtx.range_push(name)
+        try:
+            return fn(*args, **kwargs)
+        finally:
+            torch.cuda.nvtx.range_pop()
+    return wrapped
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -152,6 +184,7 @@ def raise_on_status(status: torch.Tensor, allow: int = 0) -> int:
     return word
 
 
+@_nvtx
 def grpo_head_forward(H, W, targets, mask, *, old_logp=None, ref_logp=None, adv=None, seq_id=None,
                       num_seqs: int = 0, eps_low: float = 0.2, eps_high: float = 0.2, beta: float = 0.0,
                       reduction: str = "token_mean", norm: float = 0.0, delta: float = 0.0,
@@ -234,6 +267,7 @@ def vocab_shard_bounds(V_total: int, num_shards: int):
     return out
 
 
+@_nvtx
 def grpo_head_logprob_shard(H, W_shard, targets, mask, *, vocab_start: int, V_total: int, row_tile: int = 0,
                             status: Optional[torch.Tensor] = None):
     """One vocabulary shard's split partials (part_m, part_s [S_shard, N]) and
@@ -252,6 +286,7 @@ def grpo_head_logprob_shard(H, W_shard, targets, mask, *, vocab_start: int, V_to
     return dict(part_m=part_m, part_s=part_s, zy=zy, status=st)
 
 
+@_nvtx
 def grpo_logprob_merge(part_m, part_s, zy, shard_starts, targets, mask, *, V_total: int,
                        status: Optional[torch.Tensor] = None):
     """logp, lse [N] from the gathered shard partials (concatenated in shard
@@ -278,6 +313,7 @@ def grpo_logprob_merge(part_m, part_s, zy, shard_starts, targets, mask, *, V_tot
     return dict(logp=logp, lse=lse, status=st)
 
 
+@_nvtx
 def grpo_head_backward_shard(H, W_shard, targets, mask, lse, coef, *, vocab_start: int, V_total: int,
                              grad_out=None, dW=None, accumulate_dW: bool = False, row_tile: int = 0,
                              status: Optional[torch.Tensor] = None):
@@ -305,6 +341,7 @@ def grpo_head_backward_shard(H, W_shard, targets, mask, lse, coef, *, vocab_star
     return dict(dH_partial=dHp, dW=dW, status=st)
 
 
+@_nvtx
 def grpo_dh_merge(dH_partials, dtype=torch.bfloat16, status: Optional[torch.Tensor] = None):
     """dH = sum over shards (in order) of the gathered fp32 partials [P, N, D]."""
     P, N, D = dH_partials.shape
@@ -318,6 +355,7 @@ def grpo_dh_merge(dH_partials, dtype=torch.bfloat16, status: Optional[torch.Tens
     return dH
 
 
+@_nvtx
 def grpo_loss_from_sequence_totals(seq_policy, seq_kl, seq_count, *, reduction: str = "token_mean",
                                    norm: float = 0.0, beta: float = 0.0, status: Optional[torch.Tensor] = None):
     """(loss, policy_loss, kl) from per-sequence totals gathered in global
@@ -336,6 +374,7 @@ def grpo_loss_from_sequence_totals(seq_policy, seq_kl, seq_count, *, reduction: 
     return dict(loss3=loss3, status=st)
 
 
+@_nvtx
 def gspo_segment_loss(logp, old_logp, mask, seg_id, num_segments: int, seg_adv, *, eps_low: float,
                       eps_high: float, divisor: float, token_weighted: bool = False, ref_logp=None,
                       beta: float = 0.0, status: Optional[torch.Tensor] = None,
@@ -370,6 +409,7 @@ def gspo_segment_loss(logp, old_logp, mask, seg_id, num_segments: int, seg_adv, 
     return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, num_clipped=clipped, status=st)
 
 
+@_nvtx
 def gspo_segment_partials(logp, old_logp, mask, seg_id, num_segments: int, *, ref_logp=None,
                           status: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
     """One sequence-parallel rank's GSPO partials: fsum [2S + 1], cnt [S + 1]."""
@@ -390,6 +430,7 @@ def gspo_segment_partials(logp, old_logp, mask, seg_id, num_segments: int, *, re
     return dict(fsum=fsum, cnt=cnt, status=st)
 
 
+@_nvtx
 def gspo_segment_loss_from_partials(logp, mask, seg_id, num_segments: int, fsum_all, cnt_all, seg_adv, *,
                                     eps_low: float, eps_high: float, divisor: float, token_weighted: bool = False,
                                     ref_logp=None, beta: float = 0.0, status: Optional[torch.Tensor] = None,
@@ -424,6 +465,7 @@ def gspo_segment_loss_from_partials(logp, mask, seg_id, num_segments: int, fsum_
     return dict(loss=loss, seg_ratio=ratio, coef=coef, mean_logp=mean_logp, num_clipped=clipped, status=st)
 
 
+@_nvtx
 def grpo_head_backward(H, W, targets, mask, lse, coef, *, grad_out=None, dH=None, dW=None,
                        accumulate_dW: bool = False, row_tile: int = 0, status: Optional[torch.Tensor] = None,
                        workspace: Optional[torch.Tensor] = None):
@@ -459,6 +501,7 @@ def grpo_head_backward(H, W, targets, mask, lse, coef, *, grad_out=None, dH=None
     return dict(dH=dH, dW=dW, status=st)
 
 
+@_nvtx
 def grpo_group_advantage(rewards, group_size: int, eps: float = 1e-4, status: Optional[torch.Tensor] = None):
     """Group-normalised advantages of per-sequence rewards."""
     _need(rewards, "rewards", _F32)

@@ -53,6 +53,26 @@ def main():
                 assert int(r["status"].item()) == 0
                 out[f"grpo/{red}/{norm}/{level}/{delta}"] = _digest(
                     [r[k] for k in ("loss3", "coef", "seq_policy", "seq_kl", "seq_count", "num_clipped")])
+    # 8192 tokens (64 sequences of 128): more than the folding CTA writes coef
+    # for, so a normaliser taken from the call uses the token-parallel coef kernel
+    w = make_workload(cfg, N=8192, old_noise=0.5)
+    Hd, Wd, y, m = dev_head(w)
+    base = g.grpo_head_forward(Hd, Wd, y, m)
+    lp = base["logp"].cpu().numpy().astype(np.float64)
+    old = dev_tensor((lp + w["u_old"]).astype(np.float32))
+    ref = dev_tensor((lp + w["u_ref"]).astype(np.float32))
+    adv = dev_tensor(np.linspace(-1.2, 0.9, w["num_seqs"]).astype(np.float32))
+    seq = dev_tensor(w["seq_id"])
+    for red in ("token_mean", "seq_mean"):
+        for level in ("token", "sequence"):
+            r = g.grpo_head_forward(Hd, Wd, y, m, old_logp=old, ref_logp=ref, adv=adv, seq_id=seq,
+                                    num_seqs=w["num_seqs"], eps_low=cfg.eps_low, eps_high=cfg.eps_high,
+                                    beta=cfg.beta, reduction=red, ratio_level=level, seq_totals=True,
+                                    clip_count=True)
+            torch.cuda.synchronize()
+            assert int(r["status"].item()) == 0
+            out[f"grpo8192/{red}/{level}"] = _digest(
+                [r[k] for k in ("loss3", "coef", "seq_policy", "seq_kl", "seq_count", "num_clipped")])
     # GSPO on the packed layout (masked tokens, the -1 tail), with the KL term,
     # and its sequence-parallel pair over three pieces
     cfg = CONFIGS[3]
