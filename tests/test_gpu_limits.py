@@ -107,3 +107,27 @@ def test_host_side_refusals(gpu_lib):
     with pytest.raises(_abi.GhError, match="fixed reduction"):
         g.grpo_head_forward(H, W, y, m, old_logp=z, ref_logp=z, adv=torch.zeros(1, device="cuda"), seq_id=seq,
                             num_seqs=1, reduction="fixed")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_nonfinite_input_is_flagged_and_contained(gpu_lib, dtype):
+    # a NaN in one row of H (a poisoned input made on the host) sets the
+    # non-finite status bit and gives that row a non-finite LSE (fmax ignores
+    # NaN, so its split maxima stay -inf); every other row's logp and LSE keep
+    # the bits of the clean call
+    import gspo_logprob_gb300 as g
+    from synth import CONFIGS, make_workload
+    w = make_workload(CONFIGS[1], dtype=dtype, N=300)
+    Hd, Wd, y, m = dev_head(w)
+    clean = g.grpo_head_forward(Hd, Wd, y, m)
+    bad = Hd.clone()
+    bad[37, 11] = float("nan")
+    pois = g.grpo_head_forward(bad, Wd, y, m)
+    torch.cuda.synchronize()
+    assert int(clean["status"].item()) == 0
+    assert int(pois["status"].item()) & 2          # GH_DEV_NONFINITE
+    assert not math.isfinite(float(pois["lse"][37].item()))
+    keep = torch.ones(300, dtype=torch.bool, device="cuda")
+    keep[37] = False
+    assert torch.equal(pois["lse"][keep].view(torch.int32), clean["lse"][keep].view(torch.int32))
+    assert torch.equal(pois["logp"][keep].view(torch.int32), clean["logp"][keep].view(torch.int32))
