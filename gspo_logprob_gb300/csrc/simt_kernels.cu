@@ -223,29 +223,31 @@ __global__ void __launch_bounds__(ROWS * 4, 2) f32_dlogits_kernel(
 // C[row_off + m, n] (+)= sum_k A(m, k) B(k, n) with B n-contiguous (B(k, n) =
 // B[k sbk + n]) and A either k-contiguous (A(m, k) = A[m sam + k]: dH = G W)
 // or m-contiguous (A(m, k) = A[m + k sak]: dW = G^T H).  A TILE x TILE output
-// tile per CTA of (TILE / 8)^2 threads (128: 256 threads for large grids, 64:
-// 64 threads for small ones); thread (tr, tc) owns rows 4tr.., TILE/2 + 4tr..
-// and columns 4tc.., TILE/2 + 4tc...  The tile size changes no output's
-// arithmetic.
+// tile per CTA of (TILE / RPT)^2 threads, each owning RPT x RPT outputs:
+// rows 4tr.. (and TILE/2 + 4tr.. when RPT = 8), columns alike.  Neither the
+// tile nor the outputs per thread change any output's arithmetic.
 constexpr int G_BK = 16;
 
-template <int TILE, bool A_KCONTIG, bool VEC>
-__global__ void __launch_bounds__((TILE / 8) * (TILE / 8), TILE == 128 ? 2 : 4) f32_gemm_kernel(F32GemmArgs a) {
-  constexpr int THREADS = (TILE / 8) * (TILE / 8);
-  constexpr int TPR = TILE / 8;        // threads per row of the thread grid
+template <int TILE, int RPT, bool A_KCONTIG, bool VEC>
+__global__ void __launch_bounds__((TILE / RPT) * (TILE / RPT), 2) f32_gemm_kernel(F32GemmArgs a) {
+  constexpr int THREADS = (TILE / RPT) * (TILE / RPT);
+  constexpr int TPR = TILE / RPT;      // threads per row of the thread grid
   constexpr int Q = TILE * 4 / THREADS;  // float4 of each operand chunk per thread
   constexpr int F4R = TILE / 4;        // float4 per k-row of an MN-contiguous chunk
   constexpr int PAD = TILE + 4;
+  static_assert(RPT == 4 || RPT == 8, "4 x 4 or 8 x 8 outputs per thread");
   __shared__ __align__(16) float As[2][G_BK][PAD];
   __shared__ __align__(16) float Bs[2][G_BK][PAD];
   const int t = threadIdx.x;
   const int tr = t / TPR, tc = t % TPR;
   const int m0 = blockIdx.y * TILE, n0 = blockIdx.x * TILE;
-  float acc[8][8];
+  // output i of the thread's RPT rows (columns alike): 4tr + i, and with 8 per
+  // thread the second four at TILE / 2 + 4tr
+  float acc[RPT][RPT];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < RPT; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < RPT; ++j) acc[i][j] = 0.f;
 
   float4 pa[Q], pb[Q];
   // A chunk: TILE x 16.  k-contiguous: element e = t + THREADS q -> row e/4,
@@ -306,14 +308,14 @@ __global__ void __launch_bounds__((TILE / 8) * (TILE / 8), TILE == 128 ? 2 : 4) 
   // parallel wave the partial goes to this slice's scratch slab instead
   auto flush = [&](int s) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RPT; ++i) {
       const int gm = m0 + (i < 4 ? 4 * tr : TILE / 2 + 4 * tr) + (i & 3);
       if (gm >= a.M) continue;
       float* crow = wave ? a.scratch + (static_cast<long long>(blockIdx.z) * a.M + gm) * a.Nn
                          : a.C + (static_cast<long long>(a.row_off) + gm) * a.ldc;
       const bool add = !wave && (s > 0 || a.accumulate);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < RPT; ++j) {
         const int gn = n0 + (j < 4 ? 4 * tc : TILE / 2 + 4 * tc) + (j & 3);
         if (gn >= a.Nn) continue;
         crow[gn] = add ? crow[gn] + acc[i][j] : acc[i][j];
@@ -329,23 +331,34 @@ __global__ void __launch_bounds__((TILE / 8) * (TILE / 8), TILE == 128 ? 2 : 4) 
     if (kc + 1 < nk) fetch(k_beg + (kc + 1) * G_BK, k_end);
 #pragma unroll
     for (int k = 0; k < G_BK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * tr]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][TILE / 2 + 4 * tr]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][4 * tc]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][TILE / 2 + 4 * tc]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      if constexpr (RPT == 8) {
+        const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * tr]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][k][TILE / 2 + 4 * tr]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][4 * tc]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][k][TILE / 2 + 4 * tc]);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      } else {
+        const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][k][4 * tr]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][k][4 * tc]);
+        const float av[4] = {a0.x, a0.y, a0.z, a0.w};
+        const float bv[4] = {b0.x, b0.y, b0.z, b0.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      }
     }
     if ((kc + 1) % CPS == 0 || kc + 1 == nk) {
       flush(s_beg + kc / CPS);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < RPT; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < RPT; ++j) acc[i][j] = 0.f;
     }
     if (kc + 1 < nk) {
       stash(buf ^ 1);
@@ -411,9 +424,10 @@ cudaError_t launch_dlogits_f32(const F32DlogitsArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Output tile of an M x Nn fp32 GEMM: 128 x 128 unless that leaves fewer
-// CTAs than a GB300 has SMs (152; a constant, so nothing here depends on the
-// machine), then 64 x 64.
+// Output tile of an M x Nn fp32 GEMM: 128 x 128 (256 threads, 8 x 8 outputs
+// each) unless that leaves fewer CTAs than a GB300 has SMs (152; a constant,
+// so nothing here depends on the machine), then 64 x 64 (256 threads, 4 x 4
+// outputs each: four times the warps on a small output).
 static int gemm_f32_tile(long long M, long long Nn) {
   return ceil_div(M, 128) * ceil_div(Nn, 128) < 152 ? 64 : 128;
 }
@@ -434,20 +448,20 @@ int gemm_f32_par(long long M, long long Nn, long long K, size_t scratch_bytes) {
   return p > 1 ? static_cast<int>(p) : 1;
 }
 
-template <int TILE>
+template <int TILE, int RPT>
 static void gemm_f32_launch(const F32GemmArgs& a, unsigned count, bool kc, bool vec, cudaStream_t st) {
-  constexpr int THREADS = (TILE / 8) * (TILE / 8);
+  constexpr int THREADS = (TILE / RPT) * (TILE / RPT);
   dim3 grid(static_cast<unsigned>(ceil_div(a.Nn, TILE)), static_cast<unsigned>(ceil_div(a.M, TILE)), count);
   if (kc) {
     if (vec)
-      f32_gemm_kernel<TILE, true, true><<<grid, THREADS, 0, st>>>(a);
+      f32_gemm_kernel<TILE, RPT, true, true><<<grid, THREADS, 0, st>>>(a);
     else
-      f32_gemm_kernel<TILE, true, false><<<grid, THREADS, 0, st>>>(a);
+      f32_gemm_kernel<TILE, RPT, true, false><<<grid, THREADS, 0, st>>>(a);
   } else {
     if (vec)
-      f32_gemm_kernel<TILE, false, true><<<grid, THREADS, 0, st>>>(a);
+      f32_gemm_kernel<TILE, RPT, false, true><<<grid, THREADS, 0, st>>>(a);
     else
-      f32_gemm_kernel<TILE, false, false><<<grid, THREADS, 0, st>>>(a);
+      f32_gemm_kernel<TILE, RPT, false, false><<<grid, THREADS, 0, st>>>(a);
   }
 }
 
@@ -473,9 +487,9 @@ cudaError_t launch_gemm_f32(const F32GemmArgs& a0, cudaStream_t st) {
     const int count = par > 1 ? (slices - s0 < par ? slices - s0 : par) : 1;
     a.slice0 = s0;
     if (tile == 64)
-      gemm_f32_launch<64>(a, static_cast<unsigned>(count), kc, vec, st);
+      gemm_f32_launch<64, 4>(a, static_cast<unsigned>(count), kc, vec, st);
     else
-      gemm_f32_launch<128>(a, static_cast<unsigned>(count), kc, vec, st);
+      gemm_f32_launch<128, 8>(a, static_cast<unsigned>(count), kc, vec, st);
     if (!first) count_extra_launch();
     first = false;
     if (par > 1) {

@@ -8,8 +8,12 @@
 // MMAs of tile i+1).
 //
 //   both CTAs: warp 0 TMA producer (its A rows and B half; completion is
-//              signalled on the even CTA's stage barrier), warps 2..5 epilogue
-//              (its 128 rows; frees the accumulator on the even CTA's barrier)
+//              signalled on the even CTA's stage barrier), warps 2.. epilogue
+//              (its 128 rows; frees the accumulator on the even CTA's barrier):
+//              EG groups of four warps, group g taking every EG-th tile of the
+//              pair in accumulator g (EG = 2 runs two tiles' epilogues at once
+//              when one epilogue outlasts a tile's MMAs; every row's arithmetic
+//              is the same either way)
 //   even CTA : warp 1 issues the pair MMAs and commits them to both CTAs'
 //              stage-free and accumulator-full barriers (multicast)
 //   both CTAs: warp 1 allocates / frees TMEM collectively (cta_group::2)
@@ -31,8 +35,11 @@ struct TcPairCfg {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 };
 
-template <bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(TcPairCfg::THREADS, 1)
+// threads of a pair kernel CTA with EG epilogue groups
+constexpr int tc_pair_threads(int EG) { return 64 + 32 * TcPairCfg::EPI_WARPS * EG; }
+
+template <bool A_MN, bool B_MN, class Epi, int EG = 1>
+__global__ void __launch_bounds__(tc_pair_threads(EG), 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const TcSched sc, const int b_off_n, const int b_off_k, const typename Epi::Params ep,
                         int* status, const uint64_t timeout_ns) {
@@ -185,14 +192,20 @@ __global__ void __launch_bounds__(TcPairCfg::THREADS, 1)
     }
   } else {
     // -------------------------------------------------- epilogue warps (both CTAs)
+    // TMEM lane quadrant = warp id mod 4; group grp takes this pair's tasks
+    // j = grp, grp + EG, ... (one tile each when EG > 1) in accumulator grp
+    static_assert(EG == 1 || EG == 2, "one or two epilogue groups");
     const int sub = warp & 3;
+    const int grp = EG == 1 ? 0 : (warp - 2) / TcPairCfg::EPI_WARPS;
     const int row = static_cast<int>(rank) * TC_BM + sub * 32 + lane;  // row within the 256-row tile
     const uint32_t lane_addr = static_cast<uint32_t>(sub * 32) << 16;
-    int acc = 0;
+    int acc = grp;
     uint32_t acc_phase = 0;
     bool ok = true;
     Epi epi;
-    for (int task = cid; ok && task < sc.num_tasks; task += ncl) {
+    int j = 0;
+    for (int task = cid; ok && task < sc.num_tasks; task += ncl, ++j) {
+      if (EG > 1 && j % EG != grp) continue;
       int m_blk, ng;
       tc_task_of(sc, task, m_blk, ng);
       epi.begin_task(ep, sc, m_blk, row);
@@ -214,8 +227,12 @@ __global__ void __launch_bounds__(TcPairCfg::THREADS, 1)
           else
             mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
         }
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (EG == 1) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        } else {
+          acc_phase ^= 1u;  // this group's accumulator, next use
+        }
       }
       if (ok) epi.end_task(ep, sc, m_blk, ng, row);
     }

@@ -64,6 +64,15 @@ int fwd_group_m() {
   static const int v = env_int("GH_FWD_GROUP_M", 16);
   return v > 0 ? v : 0;
 }
+// forward epilogue groups of the CTA-pair kernel: 2 (two tiles' epilogues at
+// once) when a tile's MMAs are short next to its epilogue -- K of at most 16
+// blocks (D <= 1024) -- else 1; GH_FWD_EPI_GROUPS = 1 or 2 forces it.  The
+// results are the same bits either way.
+int fwd_epi_groups(int num_kb) {
+  static const int v = env_int("GH_FWD_EPI_GROUPS", 0);
+  if (v == 1 || v == 2) return v;
+  return num_kb <= 16 ? 2 : 1;
+}
 int dlogits_group_m() {
   static const int v = kind_group_m("GH_DLOGITS_GROUP_M", 16);
   return v;
@@ -181,20 +190,22 @@ int max_pairs() {
   return cache[dev];
 }
 
-template <bool A_MN, bool B_MN, class Epi>
+template <bool A_MN, bool B_MN, class Epi, int EG = 1>
 cudaError_t launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const TcSched& sc, int b_off_n, int b_off_k,
                            const typename Epi::Params& ep, int* status, cudaStream_t st) {
   using C = TcPairCfg;
-  auto kern = tc_gemm_pair_kernel<A_MN, B_MN, Epi>;
+  constexpr int THREADS = tc_pair_threads(EG);
+  if (EG > 1 && sc.n_per_task != 1) return cudaErrorInvalidValue;  // groups take whole tasks of one tile
+  auto kern = tc_gemm_pair_kernel<A_MN, B_MN, Epi, EG>;
   static KernSetup setup;  // per instantiation
   int pairs_fit = 0;
-  cudaError_t e0 = kern_setup(setup, reinterpret_cast<const void*>(kern), C::SMEM_BYTES, C::THREADS, true, &pairs_fit);
+  cudaError_t e0 = kern_setup(setup, reinterpret_cast<const void*>(kern), C::SMEM_BYTES, THREADS, true, &pairs_fit);
   if (e0 != cudaSuccess) return e0;
   if (sc.num_tasks <= 0) return cudaSuccess;
   const int pairs = sc.num_tasks < pairs_fit ? sc.num_tasks : pairs_fit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(C::THREADS);
+  cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -253,6 +264,7 @@ cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st) {
     CUtensorMap tb2;  // each CTA of the pair stages 128 of the 256 columns
     if (!make_tmap_bf16(&tb2, a.W, a.D, a.V, static_cast<uint64_t>(a.D) * 2, TC_BK, TC_BN / 2))
       return cudaErrorInvalidValue;
+    if (fwd_epi_groups(nkb) == 2) return launch_tc_pair<false, false, EpiFwdLse, 2>(ta, tb2, sc, 0, 0, ep, a.status, st);
     return launch_tc_pair<false, false, EpiFwdLse>(ta, tb2, sc, 0, 0, ep, a.status, st);
   }
   return launch_tc<2, 1, false, false, EpiFwdLse>(ta, tb, sc, 0, 0, ep, a.status, st);

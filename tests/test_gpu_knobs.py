@@ -73,3 +73,13 @@ def test_forward_bits_do_not_depend_on_raster(gpu_lib):
     for g in ("1", "3", "0"):
         other = _child({"GH_FWD_GROUP_M": g})
         assert (other["lse"], other["logp"]) == (base["lse"], base["logp"]), g
+
+
+def test_forward_bits_do_not_depend_on_epilogue_groups(gpu_lib):
+    # one or two groups of epilogue warps in the forward's CTA-pair kernel only
+    # change how many tiles' epilogues run at once; every row's arithmetic is
+    # the same (D = 192 here, so the default is two groups)
+    base = _child({})
+    for g in ("1", "2"):
+        other = _child({"GH_FWD_EPI_GROUPS": g})
+        assert (other["lse"], other["logp"]) == (base["lse"], base["logp"]), g
