@@ -388,14 +388,16 @@ gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* log
     if (e != cudaSuccess) return cuda_fail(e, "forward logits/LSE launch");
     e = run(K_MERGE, st, [&] {
       return launch_merge(N, V, static_cast<int>(num_splits(V)), w.part_m, w.part_s, w.zy, head->targets, head->mask,
-                          logp, lse, status, st);
+                          logp, lse, status, grpo ? w.loss : nullptr, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   if (grpo) {
+    // with N > 0 the merge above was given this scratch and zeroed its control words
     void* scratch = (ws && N > 0) ? fwd_layout(head, ws).loss : nullptr;
-    cudaError_t e =
-        run(K_GRPO, st, [&] { return launch_grpo(N, logp, head->mask, grpo, coef, loss3, status, scratch, st); });
+    cudaError_t e = run(K_GRPO, st, [&] {
+      return launch_grpo(N, logp, head->mask, grpo, coef, loss3, status, scratch, scratch != nullptr, st);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "GRPO loss launch");
   }
   return GH_OK;
@@ -655,8 +657,9 @@ static gh_status backward_impl(const gh_head* head, const float* lse, const floa
       const int ldg = static_cast<int>(w.vb);
       cudaError_t e;
       if (bf16) {
-        TcDlogitsArgs da{n, D, V, vb0, width, ldg, Hc, head->W, yc, lse_c, coef_c, grad_out, w.G, status,
-                         col_offset};
+        // the dlogits launch zeroes the fused launch's tile counter on entry
+        TcDlogitsArgs da{n,   D,      V,          vb0, width, ldg, Hc, head->W, yc, lse_c, coef_c, grad_out, w.G,
+                         status, col_offset, dhdw_fused() ? w.task_ctr : nullptr};
         e = run(K_DLOGITS_TC, st, [&] { return launch_dlogits_tc(da, st); });
         if (e != cudaSuccess) return cuda_fail(e, "dlogits launch");
         int mode;
@@ -676,7 +679,7 @@ static gh_status backward_impl(const gh_head* head, const float* lse, const floa
         TcDhArgs ha{n, D, V, vb0, width, ldg, w.G, head->W, mode, acc32, dHc, status};
         TcDwArgs wa{n, D, V, vb0, width, ldg, w.G, Hc, acc_dW, dW, status};
         if (dhdw_fused()) {
-          e = run(K_DHDW_TC, st, [&] { return launch_dhdw_tc(ha, wa, w.task_ctr, st); });
+          e = run(K_DHDW_TC, st, [&] { return launch_dhdw_tc(ha, wa, w.task_ctr, true, st); });
           if (e != cudaSuccess) return cuda_fail(e, "dH/dW launch");
         } else {
           e = run(K_DH_TC, st, [&] { return launch_dh_tc(ha, st); });

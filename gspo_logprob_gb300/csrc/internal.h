@@ -85,6 +85,7 @@ struct TcDlogitsArgs {
   void* G;
   int* status;
   int col_offset;
+  int* zero_word;  // nullable: set to 0 by the launch (the fused dH/dW tile counter that follows)
 };
 cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st);
 
@@ -109,10 +110,12 @@ struct TcDwArgs {  // dW[vb0:vb0+width] (+)= G[:, :width]^T H
 };
 cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st);
 // dH and dW of one vocabulary block in one launch of CTA pairs with tiles
-// handed out from *task_ctr (a device int the call zeroes first).  Used when
+// handed out from *task_ctr, which must read 0 when the launch starts: the
+// call zeroes it first unless ctr_zeroed says an earlier launch on the same
+// stream (the dlogits launch given it as zero_word) already did.  Used when
 // dhdw_fused() (the CTA-pair kernels are on and GH_BWD_FUSED is not 0).
 bool dhdw_fused();
-cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, cudaStream_t st);
+cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, bool ctr_zeroed, cudaStream_t st);
 
 // --- fp32 SIMT launchers (simt_kernels.cu) ----------------------------------
 struct F32FwdArgs {
@@ -175,9 +178,11 @@ int gemm_f32_par(long long M, long long Nn, long long K, size_t scratch_bytes);
 void count_extra_launch();
 
 // --- loss kernels (loss_kernels.cu) -----------------------------------------
+// grpo_scratch (nullable): the scratch of the GRPO loss launched next on the
+// same stream, whose control words the merge zeroes.
 cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const float* part_s, const float* zy,
                          const int32_t* targets, const uint8_t* mask, float* logp, float* lse, int* status,
-                         cudaStream_t st);
+                         void* grpo_scratch, cudaStream_t st);
 // Shard bounds (global vocabulary ids, num_shards + 1 entries) for the merge of
 // vocabulary-parallel partials; zy is [num_shards, N].
 constexpr int MAX_SHARDS = 64;
@@ -191,9 +196,10 @@ cudaError_t launch_merge_shards(int N, int V_total, int splits, const float* par
 // GRPO loss.  `scratch` (nullable): grpo_loss_scratch_bytes(N) bytes from the
 // forward workspace; with it, and at most grpo_loss_scratch_seqs(N) sequences,
 // the loss runs one CTA per sequence, otherwise one CTA over all of them (the
-// same bits either way).
+// same bits either way).  ctl_zeroed: the merge before it on the stream was
+// given the same scratch and zeroed its control words (else the call does).
 cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_grpo* g, float* coef,
-                        float* loss3, int* status, void* scratch, cudaStream_t st);
+                        float* loss3, int* status, void* scratch, bool ctl_zeroed, cudaStream_t st);
 size_t grpo_loss_scratch_bytes(int64_t N);
 int64_t grpo_loss_scratch_seqs(int64_t N);
 cudaError_t launch_grpo_totals(int num_seqs, const float* seq_policy, const float* seq_kl, const int32_t* seq_count,

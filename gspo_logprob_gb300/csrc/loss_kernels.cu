@@ -17,6 +17,8 @@ namespace gh {
 
 namespace {
 
+constexpr int GRPO_CTL_WORDS = 8;  // control words of the multi-CTA GRPO loss
+
 __device__ __forceinline__ float wsum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -86,7 +88,9 @@ __global__ void __launch_bounds__(256) merge_kernel(int N, int V, int splits, co
                                                     const float* __restrict__ part_s, const float* __restrict__ zy,
                                                     const int* __restrict__ targets,
                                                     const uint8_t* __restrict__ mask, float* logp, float* lse,
-                                                    int* status) {
+                                                    int* status, int* zero_ctl) {
+  // the control words of the multi-CTA GRPO loss launched next on the stream
+  if (zero_ctl && blockIdx.x == 0 && threadIdx.x < GRPO_CTL_WORDS) zero_ctl[threadIdx.x] = 0;
   __shared__ float red[8][33];
   const float L = fold_splits(N, splits, part_m, part_s, red);
   const int i = blockIdx.x * 32 + (threadIdx.x & 31);
@@ -852,12 +856,20 @@ __global__ void timeout_probe_kernel(int* status, uint64_t timeout_ns) {
 
 }  // namespace
 
+// The control words inside the GRPO loss's scratch: after the four per-sequence
+// arrays of grpo_loss_scratch_seqs(N) entries, each 256-byte aligned.
+static int* grpo_scratch_ctl(void* scratch, int64_t N) {
+  const size_t a = align_up(static_cast<size_t>(grpo_loss_scratch_seqs(N)) * 4, 256);
+  return reinterpret_cast<int*>(static_cast<char*>(scratch) + 4 * a);
+}
+
 cudaError_t launch_merge(int N, int V, int splits, const float* part_m, const float* part_s, const float* zy,
                          const int32_t* targets, const uint8_t* mask, float* logp, float* lse, int* status,
-                         cudaStream_t st) {
+                         void* grpo_scratch, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
+  int* ctl = grpo_scratch ? grpo_scratch_ctl(grpo_scratch, N) : nullptr;
   merge_kernel<<<static_cast<unsigned>(ceil_div(N, 32)), 256, 0, st>>>(N, V, splits, part_m, part_s, zy, targets,
-                                                                        mask, logp, lse, status);
+                                                                        mask, logp, lse, status, ctl);
   return cudaGetLastError();
 }
 
@@ -896,7 +908,7 @@ static bool loss_one_cta_knob() {
 }
 
 cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_grpo* g, float* coef, float* loss3,
-                        int* status, void* scratch, cudaStream_t st) {
+                        int* status, void* scratch, bool ctl_zeroed, cudaStream_t st) {
   GrpoP p;
   p.N = N;
   p.logp = logp;
@@ -931,8 +943,9 @@ cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_
     gs.K = reinterpret_cast<float*>(b + a);
     gs.R = reinterpret_cast<float*>(b + 2 * a);
     gs.n = reinterpret_cast<int*>(b + 3 * a);
-    gs.ctl = reinterpret_cast<int*>(b + 4 * a);
-    cudaError_t e = cudaMemsetAsync(gs.ctl, 0, 8 * sizeof(int), st);
+    gs.ctl = grpo_scratch_ctl(scratch, N);
+    cudaError_t e = cudaSuccess;
+    if (!ctl_zeroed) e = cudaMemsetAsync(gs.ctl, 0, GRPO_CTL_WORDS * sizeof(int), st);
     if (e != cudaSuccess) return e;
     grpo_loss_kernel<false><<<loss_grid(S), LB, 0, st>>>(p, gs);
     e = cudaGetLastError();

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(TcCfg<MT, CG>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) Epi::on_entry(ep);  // before any wait that may abort
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -311,6 +312,7 @@ struct EpiFwdLse {
     const int* targets;
     int col_offset;  // global vocabulary id of local column 0 (vocabulary shards)
   };
+  static __device__ __forceinline__ void on_entry(const Params&) {}
   float m, s;
   int y, grow;
   bool valid;
@@ -392,7 +394,11 @@ struct EpiDlogits {
     const int* targets;
     int col_offset;  // global vocabulary id of local column 0 (vocabulary shards)
     __nv_bfloat16* G;
+    int* zero_word;  // nullable: set to 0 on entry (the next launch's tile counter)
   };
+  static __device__ __forceinline__ void on_entry(const Params& p) {
+    if (p.zero_word) *p.zero_word = 0;
+  }
   __device__ __forceinline__ void begin_task(const Params&, const TcSched&, int, int) {}
   __device__ __forceinline__ void end_task(const Params&, const TcSched&, int, int, int) {}
 
@@ -445,6 +451,7 @@ struct EpiStore {
     float* out32;
     __nv_bfloat16* out16;
   };
+  static __device__ __forceinline__ void on_entry(const Params&) {}
   __device__ __forceinline__ void begin_task(const Params&, const TcSched&, int, int) {}
   __device__ __forceinline__ void end_task(const Params&, const TcSched&, int, int, int) {}
 

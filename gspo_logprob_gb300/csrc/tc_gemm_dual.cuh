@@ -11,7 +11,7 @@
 // tile.
 //
 // Task hand-off inside a pair: the even CTA's producer thread draws the task
-// index (atomicAdd on *task_ctr, which the host zeroes before the launch) while
+// index (atomicAdd on *task_ctr, zeroed before the launch) while
 // the last 16 K blocks of its current tile are still to be loaded, and
 // publishes it in a ring of DUAL_RING slots in both CTAs' shared memory (a
 // remote st.shared::cluster plus a release arrive on the peer's slot barrier).
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(TcPairCfg::THREADS, 1)
           if (!mbar_wait_cluster_bounded(&rempty[slot], rph ^ 1u, abort_flag, status, timeout_ns)) break;
           if (!have_next) next = atomicAdd(task_ctr, 1);
           have_next = false;
-          t = next < T ? next : T;
+          t = (next >= 0 && next < T) ? next : T;  // past the end (or a counter never zeroed): stop
           ring[slot] = t;
           st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&ring[slot])), 1), static_cast<uint32_t>(t));
           mbar_arrive(&rfull[slot]);

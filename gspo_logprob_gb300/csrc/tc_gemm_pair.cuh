@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(tc_pair_threads(EG), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: even CTA (issues the MMAs), 1: its peer
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  if (blockIdx.x == 0 && threadIdx.x == 0) Epi::on_entry(ep);  // before any wait that may abort
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);

@@ -285,6 +285,7 @@ cudaError_t launch_dlogits_tc(const TcDlogitsArgs& a, cudaStream_t st) {
   ep.targets = a.targets;
   ep.col_offset = a.col_offset;
   ep.G = static_cast<__nv_bfloat16*>(a.G);
+  ep.zero_word = a.zero_word;
   const int nkb = static_cast<int>(ceil_div(a.D, TC_BK));
   const int nn = static_cast<int>(ceil_div(a.width, TC_BN));
   if (dlogits_mt() == 1) {
@@ -362,7 +363,7 @@ cudaError_t launch_dw_tc(const TcDwArgs& a, cudaStream_t st) {
 
 bool dhdw_fused() { return bwd_fused_knob() == 1 && dh_pair() == 1 && dw_pair() == 1; }
 
-cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, cudaStream_t st) {
+cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, bool ctr_zeroed, cudaStream_t st) {
   // dH: A = G [N, ldg] K-major, B = W [V, D] MN-major (rows vb0.. of the block)
   CUtensorMap ta_h, tb_h, ta_w, tb_w;
   if (!make_tmap_bf16(&ta_h, h.G, h.ldg, h.N, static_cast<uint64_t>(h.ldg) * 2, TC_BK, TC_BM))
@@ -413,8 +414,10 @@ cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, 
   cudaError_t e = kern_setup(setup, reinterpret_cast<const void*>(kern), DUAL_SMEM_BYTES, TcPairCfg::THREADS, true,
                              &pairs_fit);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(task_ctr, 0, sizeof(int), st);
-  if (e != cudaSuccess) return e;
+  if (!ctr_zeroed) {
+    e = cudaMemsetAsync(task_ctr, 0, sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
   const int pairs = tasks < pairs_fit ? tasks : pairs_fit;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
