@@ -653,7 +653,7 @@ def run_aux(args, rank, world, local):
         "metric": METRIC, "value": round(N / (ms_step * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dt == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {cfg.name}, N={N}, D={D}, V={V}, step = {what}"
+        "config": {"workload": f"{args.workload}: shapes of {cfg.name}, N={N}, D={D}, V={V}, {dt}, step = {what}"
                                + (" (CUDA graph replay)" if args.graph else ""),
                    "l2": "flushed between timed steps (512 MB write outside the events)"},
         "tflops": round(flops_step / (ms_step * 1e-3) / 1e12, 2), "roofline": roof, "kernels": kernels,
