@@ -378,7 +378,9 @@ gh_status grpo_head_forward(const gh_head* head, const gh_grpo* grpo, float* log
     FwdWs w = fwd_layout(head, ws);
     cudaError_t e;
     if (head->dtype == GH_BF16) {
-      TcFwdArgs a{N, D, V, head->row_tile, head->H, head->W, head->targets, w.part_m, w.part_s, w.zy, status};
+      // tile counter of the on-demand forward: a word of the loss scratch's counter block
+      int* ctr = grpo_scratch_ctl(w.loss, N) + FWD_TILE_CTR_WORD;
+      TcFwdArgs a{N, D, V, head->row_tile, head->H, head->W, head->targets, w.part_m, w.part_s, w.zy, status, 0, ctr};
       e = run(K_FWD_TC, st, [&] { return launch_fwd_tc(a, st); });
     } else {
       F32FwdArgs a{N, D, V, head->row_tile, static_cast<const float*>(head->H), static_cast<const float*>(head->W),

@@ -71,7 +71,12 @@ struct TcFwdArgs {
   float* zy;
   int* status;
   int col_offset;  // vocabulary shards: global id of local column 0 (else 0)
+  int* task_ctr;   // nullable: a device int for tiles handed out on demand (fwd_dynamic)
 };
+// Forward logits + LSE.  With a task counter and fwd_dynamic(), the pairs take
+// tiles from *task_ctr (the call zeroes it first), so they stay within about a
+// tile of each other and a W tile is still in L2 for the rest of its raster
+// group; otherwise tiles are dealt round-robin.  The bits are the same.
 cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st);
 
 struct TcDlogitsArgs {
@@ -202,6 +207,12 @@ cudaError_t launch_grpo(int N, const float* logp, const uint8_t* mask, const gh_
                         float* loss3, int* status, void* scratch, bool ctl_zeroed, cudaStream_t st);
 size_t grpo_loss_scratch_bytes(int64_t N);
 int64_t grpo_loss_scratch_seqs(int64_t N);
+// The 256-byte block of counters at the end of that scratch: words
+// [0, GRPO_CTL_WORDS) are the loss's control words, word FWD_TILE_CTR_WORD the
+// forward's tile counter.
+constexpr int GRPO_CTL_WORDS = 8;
+constexpr int FWD_TILE_CTR_WORD = 32;
+int* grpo_scratch_ctl(void* scratch, int64_t N);
 cudaError_t launch_grpo_totals(int num_seqs, const float* seq_policy, const float* seq_kl, const int32_t* seq_count,
                                int reduction, double norm, float beta, float* loss3, int* status, cudaStream_t st);
 struct GspoArgs {

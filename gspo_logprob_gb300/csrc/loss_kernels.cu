@@ -17,8 +17,6 @@ namespace gh {
 
 namespace {
 
-constexpr int GRPO_CTL_WORDS = 8;  // control words of the multi-CTA GRPO loss
-
 __device__ __forceinline__ float wsum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -856,9 +854,9 @@ __global__ void timeout_probe_kernel(int* status, uint64_t timeout_ns) {
 
 }  // namespace
 
-// The control words inside the GRPO loss's scratch: after the four per-sequence
+// The counters inside the GRPO loss's scratch: after the four per-sequence
 // arrays of grpo_loss_scratch_seqs(N) entries, each 256-byte aligned.
-static int* grpo_scratch_ctl(void* scratch, int64_t N) {
+int* grpo_scratch_ctl(void* scratch, int64_t N) {
   const size_t a = align_up(static_cast<size_t>(grpo_loss_scratch_seqs(N)) * 4, 256);
   return reinterpret_cast<int*>(static_cast<char*>(scratch) + 4 * a);
 }

@@ -73,6 +73,13 @@ int fwd_epi_groups(int num_kb) {
   if (v == 1 || v == 2) return v;
   return num_kb <= 16 ? 2 : 1;
 }
+// forward tiles handed out on demand (1) or dealt round-robin (0); default:
+// on demand when one group of epilogue warps is used (K of more than 16 blocks)
+int fwd_dynamic(int num_kb) {
+  static const int v = env_int("GH_FWD_DYNAMIC", -1);
+  if (v == 0 || v == 1) return v;
+  return fwd_epi_groups(num_kb) == 1 ? 1 : 0;
+}
 int dlogits_group_m() {
   static const int v = kind_group_m("GH_DLOGITS_GROUP_M", 16);
   return v;
@@ -233,6 +240,44 @@ TcSched make_sched(int num_m_blocks, int num_n_blocks, int n_per_task, int num_k
   return sc;
 }
 
+// One launch of tc_dual_pair_kernel: the tiles of j0, then of j1, handed out
+// from *task_ctr, which must read 0 at the start (the call zeroes it unless
+// ctr_zeroed says an earlier launch on the stream did).
+template <class Epi>
+cudaError_t launch_dual(const CUtensorMap& ta0, const CUtensorMap& tb0, const CUtensorMap& ta1, const CUtensorMap& tb1,
+                        const PairJob& j0, const PairJob& j1, const typename Epi::Params& e0,
+                        const typename Epi::Params& e1, int* task_ctr, bool ctr_zeroed, int* status,
+                        cudaStream_t st) {
+  const int tasks = j0.sc.num_tasks + j1.sc.num_tasks;
+  if (tasks <= 0) return cudaSuccess;
+  auto kern = tc_dual_pair_kernel<Epi>;
+  static KernSetup setup;  // per instantiation
+  int pairs_fit = 0;
+  cudaError_t e = kern_setup(setup, reinterpret_cast<const void*>(kern), DUAL_SMEM_BYTES, TcPairCfg::THREADS, true,
+                             &pairs_fit);
+  if (e != cudaSuccess) return e;
+  if (!ctr_zeroed) {
+    e = cudaMemsetAsync(task_ctr, 0, sizeof(int), st);
+    if (e != cudaSuccess) return e;
+  }
+  const int pairs = tasks < pairs_fit ? tasks : pairs_fit;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(TcPairCfg::THREADS);
+  cfg.dynamicSmemBytes = DUAL_SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, ta0, tb0, ta1, tb1, j0, j1, e0, e1, task_ctr, status, timeout_ns());
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st) {
@@ -264,6 +309,16 @@ cudaError_t launch_fwd_tc(const TcFwdArgs& a, cudaStream_t st) {
     CUtensorMap tb2;  // each CTA of the pair stages 128 of the 256 columns
     if (!make_tmap_bf16(&tb2, a.W, a.D, a.V, static_cast<uint64_t>(a.D) * 2, TC_BK, TC_BN / 2))
       return cudaErrorInvalidValue;
+    if (a.task_ctr && fwd_dynamic(nkb)) {
+      static_assert(TILES_PER_SPLIT == 1, "a task is one split: the epilogue ends it with the tile's column");
+      PairJob j, none;
+      j.sc = sc;
+      j.b_off_n = j.b_off_k = 0;
+      j.a_mn = j.b_mn = 0;
+      none = j;
+      none.sc.num_tasks = 0;
+      return launch_dual<EpiFwdLse>(ta, tb2, ta, tb2, j, none, ep, ep, a.task_ctr, false, a.status, st);
+    }
     if (fwd_epi_groups(nkb) == 2) return launch_tc_pair<false, false, EpiFwdLse, 2>(ta, tb2, sc, 0, 0, ep, a.status, st);
     return launch_tc_pair<false, false, EpiFwdLse>(ta, tb2, sc, 0, 0, ep, a.status, st);
   }
@@ -403,42 +458,11 @@ cudaError_t launch_dhdw_tc(const TcDhArgs& h, const TcDwArgs& w, int* task_ctr, 
   jw.b_off_k = 0;
   jw.a_mn = 1;
   jw.b_mn = 1;
-  const int tasks = jh.sc.num_tasks + jw.sc.num_tasks;
-  if (tasks <= 0) return cudaSuccess;
-
-  using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PairJob, PairJob, EpiStore::Params,
-                        EpiStore::Params, int*, int*, uint64_t);
-  Kern kern = tc_dual_pair_kernel<EpiStore>;
-  static KernSetup setup;
-  int pairs_fit = 0;
-  cudaError_t e = kern_setup(setup, reinterpret_cast<const void*>(kern), DUAL_SMEM_BYTES, TcPairCfg::THREADS, true,
-                             &pairs_fit);
-  if (e != cudaSuccess) return e;
-  if (!ctr_zeroed) {
-    e = cudaMemsetAsync(task_ctr, 0, sizeof(int), st);
-    if (e != cudaSuccess) return e;
-  }
-  const int pairs = tasks < pairs_fit ? tasks : pairs_fit;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(TcPairCfg::THREADS);
-  cfg.dynamicSmemBytes = DUAL_SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   // the product with the deeper K (longer tiles) first: the short tiles of
   // the other fill the end of the list
   if (jw.sc.num_kb > jh.sc.num_kb)
-    e = cudaLaunchKernelEx(&cfg, kern, ta_w, tb_w, ta_h, tb_h, jw, jh, ew, eh, task_ctr, h.status, timeout_ns());
-  else
-    e = cudaLaunchKernelEx(&cfg, kern, ta_h, tb_h, ta_w, tb_w, jh, jw, eh, ew, task_ctr, h.status, timeout_ns());
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+    return launch_dual<EpiStore>(ta_w, tb_w, ta_h, tb_h, jw, jh, ew, eh, task_ctr, ctr_zeroed, h.status, st);
+  return launch_dual<EpiStore>(ta_h, tb_h, ta_w, tb_w, jh, jw, eh, ew, task_ctr, ctr_zeroed, h.status, st);
 }
 
 }  // namespace gh

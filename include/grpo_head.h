@@ -134,10 +134,11 @@ typedef struct {
 
 /*
  * Bytes of scratch `ws` grpo_head_forward needs for this problem: the split
- * partials and target logits of the log-prob, and per-sequence slots of the
- * GRPO loss for up to max(64, N / 8) sequences (capped at 16384).  With more
- * sequences than slots the loss runs on one CTA instead of one CTA per
- * sequence, with the same results, bit for bit.
+ * partials and target logits of the log-prob, per-sequence slots of the GRPO
+ * loss for up to max(64, N / 8) sequences (capped at 16384), and 256 bytes of
+ * counters (the loss's control words and the forward's tile counter, all set
+ * by the call itself).  With more sequences than slots the loss runs on one
+ * CTA instead of one CTA per sequence, with the same results, bit for bit.
  */
 size_t grpo_head_forward_workspace_size(const gh_head* head);
 /*

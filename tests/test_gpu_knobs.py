@@ -28,6 +28,7 @@ SETTINGS = [
     {"GH_FWD_PAIR": "0", "GH_DLOGITS_PAIR": "0", "GH_DH_PAIR": "0", "GH_DW_PAIR": "0"},
     {"GH_FWD_PAIR": "0", "GH_DLOGITS_PAIR": "1", "GH_DH_PAIR": "0", "GH_DW_PAIR": "1", "GH_BWD_BLOCK_COLS": "768"},
     {"GH_BWD_FUSED": "0", "GH_BWD_BLOCK_COLS": "512"},            # dH and dW as two pair launches per block
+    {"GH_FWD_DYNAMIC": "1", "GH_BWD_BLOCK_COLS": "768"},           # forward tiles on demand
 ]
 
 
@@ -83,3 +84,13 @@ def test_forward_bits_do_not_depend_on_epilogue_groups(gpu_lib):
     for g in ("1", "2"):
         other = _child({"GH_FWD_EPI_GROUPS": g})
         assert (other["lse"], other["logp"]) == (base["lse"], base["logp"]), g
+
+
+def test_forward_bits_do_not_depend_on_tile_hand_out(gpu_lib):
+    # tiles taken on demand from a counter (the default for long K) or dealt
+    # round-robin (the default here, D = 192): each tile is the same MMA chain
+    # and epilogue, whichever pair computes it
+    base = _child({"GH_FWD_DYNAMIC": "0"})
+    for env in ({"GH_FWD_DYNAMIC": "1"}, {"GH_FWD_DYNAMIC": "1", "GH_FWD_GROUP_M": "3"}):
+        other = _child(env)
+        assert (other["lse"], other["logp"]) == (base["lse"], base["logp"]), env

@@ -67,6 +67,28 @@ def test_tp_large_vocabulary_matches_oracle(gpu_lib, P):
     assert np.max(np.abs(merged["lse"].cpu().numpy() - lse_o)) < 1e-3
 
 
+@pytest.mark.parametrize("P", [2, 3])
+def test_tp_long_k_shards_equal_whole_bitwise(gpu_lib, P):
+    # D = 2048 (32 K blocks): the whole-vocabulary forward takes its tiles on
+    # demand from a counter in its workspace, the shards (no workspace) deal
+    # theirs round-robin; every tile is the same computation either way
+    import gspo_logprob_gb300 as g
+    rng = np.random.default_rng(40 + P)
+    N, D, V = 1100, 2048, 9000
+    Hf = rng.standard_normal((N, D), dtype=np.float32)
+    Wf = (rng.standard_normal((V, D)) / math.sqrt(D)).astype(np.float32)
+    y = rng.integers(0, V, N).astype(np.int32)
+    w = dict(H=f32_to_bf16_bits(Hf), W=f32_to_bf16_bits(Wf), targets=y, mask=np.ones(N, np.uint8), dtype="bf16")
+    Hd, Wd, yd, md = dev_head(w)
+    base = g.grpo_head_forward(Hd, Wd, yd, md)
+    merged, st = _tp_forward(Hd, Wd, yd, md, V, P)
+    assert st == 0 and int(base["status"].item()) == 0
+    assert torch.equal(merged["lse"].view(torch.int32), base["lse"].view(torch.int32))
+    assert torch.equal(merged["logp"].view(torch.int32), base["logp"].view(torch.int32))
+    lp_o, lse_o, _ = oracle.selected_logprob(*host_head(w), y)
+    assert np.max(np.abs(base["lse"].cpu().numpy() - lse_o)) < 3e-2
+
+
 def test_tp_out_of_range_targets(gpu_lib):
     w = make_workload(CONFIGS[1], dtype="bf16")
     y = w["targets"].copy()
