@@ -1,5 +1,6 @@
 // Two GEMMs in one launch on CTA pairs (the dH and dW products of a backward
-// vocabulary block), with 256 x 256 tiles handed out dynamically.
+// vocabulary block), with 256 x 256 tiles handed out dynamically.  The
+// long-K forward runs here too, as one job with an empty second one.
 //
 // The pair kernel of tc_gemm_pair.cuh deals tiles round-robin, so a launch of
 // 512 dH tiles over 76 pairs runs 6.74 waves and idles a quarter of the GPU

@@ -73,12 +73,15 @@ int fwd_epi_groups(int num_kb) {
   if (v == 1 || v == 2) return v;
   return num_kb <= 16 ? 2 : 1;
 }
-// forward tiles handed out on demand (1) or dealt round-robin (0); default:
-// on demand when one group of epilogue warps is used (K of more than 16 blocks)
+// forward tiles handed out on demand (1) or dealt round-robin (0).  Default:
+// on demand for K of more than 32 blocks (D > 2048), where a launch is long
+// enough for round-robin pairs to drift apart and re-read W from DRAM (at
+// D = 4096 on demand read a third of the bytes); at D = 2048 the hand-out's
+// per-tile cost was 1-2% and round-robin stayed faster.
 int fwd_dynamic(int num_kb) {
   static const int v = env_int("GH_FWD_DYNAMIC", -1);
   if (v == 0 || v == 1) return v;
-  return fwd_epi_groups(num_kb) == 1 ? 1 : 0;
+  return num_kb > 32 && fwd_epi_groups(num_kb) == 1 ? 1 : 0;
 }
 int dlogits_group_m() {
   static const int v = kind_group_m("GH_DLOGITS_GROUP_M", 16);

@@ -69,12 +69,12 @@ def test_tp_large_vocabulary_matches_oracle(gpu_lib, P):
 
 @pytest.mark.parametrize("P", [2, 3])
 def test_tp_long_k_shards_equal_whole_bitwise(gpu_lib, P):
-    # D = 2048 (32 K blocks): the whole-vocabulary forward takes its tiles on
+    # D = 2560 (40 K blocks): the whole-vocabulary forward takes its tiles on
     # demand from a counter in its workspace, the shards (no workspace) deal
     # theirs round-robin; every tile is the same computation either way
     import gspo_logprob_gb300 as g
     rng = np.random.default_rng(40 + P)
-    N, D, V = 1100, 2048, 9000
+    N, D, V = 1100, 2560, 9000
     Hf = rng.standard_normal((N, D), dtype=np.float32)
     Wf = (rng.standard_normal((V, D)) / math.sqrt(D)).astype(np.float32)
     y = rng.integers(0, V, N).astype(np.int32)
