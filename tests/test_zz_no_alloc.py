@@ -10,6 +10,7 @@ a problem too large for the array is refused before any GPU work.  It is
 named to be collected last.
 """
 import ctypes
+import dataclasses
 import math
 
 import numpy as np
@@ -27,8 +28,8 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _problem(cfg, dtype):
-    w = make_workload(cfg, dtype=dtype)
+def _problem(cfg, dtype, N=None):
+    w = make_workload(cfg, dtype=dtype, N=N)
     H, W, y, m = dev_head(w)
     N, V = H.shape[0], W.shape[0]
     old = dev_tensor((-math.log(V) + w["u_old"]).astype(np.float32))
@@ -67,10 +68,13 @@ def _call(lib, tensors, extra, num_seqs, noalloc):
 
 def test_noalloc_forward_matches_workspace_forward(gpu_lib):
     lib = gpu_lib
-    # two calls in a row on different problems (bf16 tensor-core path, then the
-    # fp32 path with a different scratch layout); each must equal the regular entry
-    for cfg, dtype in ((CONFIGS[2], "bf16"), (CONFIGS[0], "fp32")):
-        w, tensors, extra = _problem(cfg, dtype)
+    # calls in a row on different problems (bf16 tensor-core path, the fp32
+    # path with a different scratch layout, and a bf16 forward with D > 2048,
+    # whose tiles are handed out from a counter kept in the scratch); each must
+    # equal the regular entry
+    long_k = dataclasses.replace(CONFIGS[2], D=3072, V=3000)
+    for cfg, dtype, n in ((CONFIGS[2], "bf16", None), (CONFIGS[0], "fp32", None), (long_k, "bf16", 512)):
+        w, tensors, extra = _problem(cfg, dtype, n)
         want = _call(lib, tensors, extra, w["num_seqs"], noalloc=False)
         got = _call(lib, tensors, extra, w["num_seqs"], noalloc=True)
         for k in ("logp", "lse", "coef", "loss3"):
