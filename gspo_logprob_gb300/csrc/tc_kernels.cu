@@ -1,5 +1,7 @@
 // tcgen05 kernels of the bf16 path: logits + online LSE (forward), dlogits
-// recompute (backward) and the dH / dW GEMMs, all instances of tc_gemm_kernel.
+// recompute (backward) and the dH / dW GEMMs, as instances of the CTA-pair
+// kernel (tc_gemm_pair_kernel), its on-demand form with one or two jobs
+// (tc_dual_pair_kernel) and the single-CTA kernel (tc_gemm_kernel).
 #include <cstdlib>
 #include <mutex>
 
@@ -12,9 +14,11 @@ namespace gh {
 
 namespace {
 
-// Tuning knobs (read once from the environment): CTA row-tile height of each
-// backward GEMM (1 or 2 blocks of 128 rows) and the raster group size.  Every
-// setting computes the same result; they only change tile shape and order.
+// Tuning knobs (read once from the environment): which kernel runs each
+// product, its CTA row-tile height (1 or 2 blocks of 128 rows), the raster
+// group size, the epilogue warps and the tile hand-out.  Every setting
+// computes the same result; they only change tile shape, order and which
+// warps or CTAs do the work.
 int env_int(const char* name, int dflt) {
   const char* e = getenv(name);
   return e ? atoi(e) : dflt;
